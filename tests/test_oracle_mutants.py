@@ -1,0 +1,99 @@
+"""The oracle's pins have teeth: plausible mistakes planted in a copy of the
+oracle source (a wrong tie rule, a dropped rank, a reversed rank order, a
+lost sign, an off-by-one bias, a missing saturation, a wrong packet layout, an
+unrounded chunk size, a zero seed) must each fail at least one pin.
+
+Mistakes are planted only in a temporary copy of the C oracle, on the CPU.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle_formats as tf
+from tests import test_oracle_sum as ts
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sar_oracle.c")
+
+MUTANTS = {
+    "ties away from zero":
+        ("if (rest > half || (rest == half && (keep & 1))) keep += 1;",
+         "if (rest >= half) keep += 1;"),
+    "truncation instead of rounding":
+        ("if (rest > half || (rest == half && (keep & 1))) keep += 1;", ";"),
+    "last rank dropped":
+        ("for (int k = 1; k < nranks; ++k) acc = acc + orc_load(dt, in[k], i);\n        for (int j",
+         "for (int k = 1; k < nranks - 1; ++k) acc = acc + orc_load(dt, in[k], i);\n        for (int j"),
+    "reversed rank order":
+        ("float acc = orc_load(dt, in[0], i);\n        for (int k = 1; k < nranks; ++k) acc = acc + orc_load(dt, in[k], i);\n        for (int j",
+         "float acc = orc_load(dt, in[nranks - 1], i);\n        for (int k = nranks - 2; k >= 0; --k) acc = acc + orc_load(dt, in[k], i);\n        for (int j"),
+    "accumulator seeded with +0":
+        ("float acc = orc_load(dt, in[0], i);\n        for (int k = 1; k < nranks; ++k) acc = acc + orc_load(dt, in[k], i);\n        for (int j",
+         "float acc = 0.0f;\n        for (int k = 0; k < nranks; ++k) acc = acc + orc_load(dt, in[k], i);\n        for (int j"),
+    "fp16 bias off by one":
+        ("static const orc_fmt F = { 11, -14, 15 };", "static const orc_fmt F = { 11, -14, 16 };"),
+    "bf16 sign dropped":
+        ("    if (c < 0) return s | 0x7F80;                     /* overflow -> infinity */\n    return s | (uint16_t)c;",
+         "    if (c < 0) return s | 0x7F80;                     /* overflow -> infinity */\n    return (uint16_t)c;"),
+    "e4m3fn overflow to NaN":
+        ("if (c < 0 || c > 0x7E) return s | 0x7E;", "if (c < 0 || c > 0x7E) return s | 0x7F;"),
+    "fp16 subnormal scale":
+        ("mag = ldexpf((float)f, -24);", "mag = ldexpf((float)f, -25);"),
+    "e4m3fn normal scale":
+        ("else mag = ldexpf((float)(8 + f), e - 10);", "else mag = ldexpf((float)(8 + f), e - 9);"),
+    "packet flag big-endian":
+        ("(uint8_t)(epoch >> (8 * k));", "(uint8_t)(epoch >> (8 * (3 - k)));"),
+    "packet tail not zero-padded":
+        ("at < bytes ? src[at] : 0;", "at < bytes ? src[at] : 0xFF;"),
+    "chunk not rounded to a vector":
+        ("    c = (c + vec - 1) / vec * vec;\n", ""),
+    "all-gather skips a peer":
+        ("if (j == r || e == b) continue;", "if (j == r || j == 0 || e == b) continue;"),
+}
+
+
+def _battery(points):
+    """Run a selection of pins; return how many failed."""
+    checks = [
+        lambda: [tf.test_round_matches_bruteforce_nearest(points, f) for f in ("bf16", "fp16", "e4m3fn")],
+        lambda: [tf.test_decode_every_code(f) for f in ("bf16", "fp16", "e4m3fn")],
+        lambda: tf.test_golden_format_constants(),
+        lambda: [ts.test_one_rank_is_identity(d) for d in ts.DTYPES],
+        lambda: [ts.test_all_equal_inputs_give_n_times_x(d, 8) for d in ts.DTYPES],
+        lambda: [ts.test_small_integers_sum_exactly_under_any_rank_order(d, 5) for d in ts.DTYPES],
+        lambda: ts.test_all_e4m3fn_pairs_bruteforce(),
+        lambda: ts.test_rank_order_is_0_to_n_minus_1(),
+        lambda: [ts.test_rsag_chunks_partition_the_range(d) for d in ts.DTYPES],
+        lambda: [ts.test_reduce_scatter_then_all_gather_is_allreduce(d, 8, 4097) for d in ts.DTYPES],
+        lambda: [ts.test_ll_pack_byte_image(d, 5) for d in ts.DTYPES],
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, ValueError):
+            failed += 1
+    return failed
+
+
+@pytest.fixture(scope="module")
+def points():
+    return tf._f32_points()[::7]
+
+
+def test_unmodified_oracle_passes_battery(points):
+    assert _battery(points) == 0
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, points, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for '{name}' not found"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    lib = oracle.compile_library(str(path), str(tmp_path / "libmutant.so"))
+    with oracle.using_library(lib):
+        failed = _battery(points)
+    assert failed >= 1, f"no pin caught the planted mistake '{name}'"
