@@ -1,0 +1,268 @@
+// sar_api.cu -- the C ABI of libsar: argument validation, status codes and
+// dispatch from the runtime rank count to the compile-time kernel variants.
+//
+// Every unsupported input is reported before anything is launched.  In
+// "Support 2 ranks in AllreduceRsAgZeroCopy - #948" ("why") an unsupported
+// rank count made the adapter return an error without launching, which the
+// NCCL shim surfaced as ncclInvalidArgument; here the same condition is an
+// explicit SAR_ERR_UNSUPPORTED_NRANKS, and the supported set is the #948 set
+// {2, 4, 8, 16, 32} plus the trivial single rank.
+#include <cstdint>
+#include <cstring>
+
+#include "sar_internal.h"
+
+namespace sar {
+
+size_t esize_of(sar_dtype dt) {
+    switch (dt) {
+    case SAR_BF16: return 2;
+    case SAR_FP16: return 2;
+    case SAR_FP32: return 4;
+    case SAR_FP8_E4M3FN: return 1;
+    }
+    return 0;
+}
+
+namespace {
+
+bool supported_nranks(int n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32; }
+
+bool valid_dtype(int dt) { return dt >= SAR_BF16 && dt <= SAR_FP8_E4M3FN; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks nranks device pointers: non-NULL and aligned to `align`; clears
+// *all16 if any pointer is not 16-byte aligned.
+sar_status check_ptrs(const void* const* arr, int nranks, size_t align, bool* all16) {
+    for (int r = 0; r < nranks; ++r) {
+        if (arr[r] == nullptr) return SAR_ERR_INVALID_ARG;
+        if (!aligned(arr[r], align)) return SAR_ERR_MISALIGNED;
+        if (!aligned(arr[r], 16)) *all16 = false;
+    }
+    return SAR_OK;
+}
+
+// Largest count for which the byte sizes (x8 for packet buffers) fit size_t.
+bool count_fits(size_t count, size_t esize) { return count <= (SIZE_MAX / 16) / esize; }
+
+sar_status to_status(cudaError_t e) { return e == cudaSuccess ? SAR_OK : SAR_ERR_CUDA; }
+
+size_t rsag_chunk(size_t count, int nranks, sar_dtype dt) {
+    const size_t vec = 16 / esize_of(dt);
+    size_t c = (count + static_cast<size_t>(nranks) - 1) / static_cast<size_t>(nranks);
+    return (c + vec - 1) / vec * vec;
+}
+
+// Common checks of the rsag entry points.  On SAR_OK with *launch == false
+// there is nothing to do (count == 0).
+sar_status check_rsag(const void* const* in, void* const* out, int nranks, size_t count, int dtype,
+                      bool need_in, RankPtrs* p, bool* vec, bool* launch) {
+    *launch = false;
+    if (!supported_nranks(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
+    if (!valid_dtype(dtype)) return SAR_ERR_UNSUPPORTED_DTYPE;
+    if ((need_in && in == nullptr) || out == nullptr) return SAR_ERR_INVALID_ARG;
+    const size_t es = esize_of(static_cast<sar_dtype>(dtype));
+    if (!count_fits(count, es)) return SAR_ERR_INVALID_ARG;
+    if (count == 0) return SAR_OK;
+    bool all16 = true;
+    sar_status st;
+    if (need_in && (st = check_ptrs(in, nranks, es, &all16)) != SAR_OK) return st;
+    if ((st = check_ptrs(out, nranks, es,
+                         &all16)) != SAR_OK)
+        return st;
+    std::memset(p, 0, sizeof(*p));
+    for (int r = 0; r < nranks; ++r) {
+        if (need_in) p->in[r] = in[r];
+        p->out[r] = out[r];
+    }
+    *vec = all16;
+    *launch = true;
+    return SAR_OK;
+}
+
+// Common checks of the LL entry points: rank count, element type, epoch,
+// packet buffers (16-byte aligned) and the buffers of one side (`data`: the
+// inputs of pack, the outputs of unpack-reduce).  *data16 tells whether every
+// data buffer is 16-byte aligned.  On SAR_OK with *launch == false there is
+// nothing to do (count == 0).
+sar_status check_ll(const void* const* data, const void* const* pkts, int nranks, size_t count, int dtype,
+                    uint32_t epoch, bool* launch, bool* data16) {
+    *launch = false;
+    if (!supported_nranks(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
+    if (!valid_dtype(dtype)) return SAR_ERR_UNSUPPORTED_DTYPE;
+    if (data == nullptr || pkts == nullptr || epoch == 0) return SAR_ERR_INVALID_ARG;
+    const size_t es = esize_of(static_cast<sar_dtype>(dtype));
+    if (!count_fits(count, es)) return SAR_ERR_INVALID_ARG;
+    if (count == 0) return SAR_OK;
+    bool all16 = true, pk16 = true;
+    sar_status st;
+    if ((st = check_ptrs(data, nranks, es, &all16)) != SAR_OK) return st;
+    if ((st = check_ptrs(pkts, nranks, 16, &pk16)) != SAR_OK) return st;
+    *data16 = all16;
+    *launch = true;
+    return SAR_OK;
+}
+
+sar_status check_status_args(uint64_t max_spins, const int32_t* d_status) {
+    if (d_status == nullptr || max_spins == 0) return SAR_ERR_INVALID_ARG;
+    if (!aligned(d_status, 4)) return SAR_ERR_MISALIGNED;
+    return SAR_OK;
+}
+
+}  // namespace
+}  // namespace sar
+
+using namespace sar;
+
+extern "C" {
+
+SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype) {
+    if (!supported_nranks(nranks) || !valid_dtype(dtype)) return 0;
+    return rsag_chunk(count, nranks, dtype);
+}
+
+SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
+                                 sar_dtype dtype, sar_algo algo, sar_stream_t stream) {
+    if (algo != SAR_ALGO_RSAG && algo != SAR_ALGO_RSAG_TWO_PHASE) {
+        if (!supported_nranks(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
+        return SAR_ERR_INVALID_ARG;
+    }
+    RankPtrs p;
+    bool vec = false, launch = false;
+    sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
+    if (st != SAR_OK || !launch) return st;
+    const size_t chunk = rsag_chunk(count, nranks, dtype);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (algo == SAR_ALGO_RSAG) return to_status(launch_rsag(kFused, dtype, nranks, p, count, chunk, vec, s));
+    st = to_status(launch_rsag(kReduceScatter, dtype, nranks, p, count, chunk, vec, s));
+    if (st != SAR_OK) return st;
+    return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), chunk, vec, s));
+}
+
+SAR_API sar_status sar_reduce_scatter(const void* const* in, void* const* out, int nranks, size_t count,
+                                      sar_dtype dtype, sar_stream_t stream) {
+    RankPtrs p;
+    bool vec = false, launch = false;
+    sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
+    if (st != SAR_OK || !launch) return st;
+    return to_status(launch_rsag(kReduceScatter, dtype, nranks, p, count, rsag_chunk(count, nranks, dtype), vec,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API sar_status sar_all_gather(void* const* out, int nranks, size_t count, sar_dtype dtype,
+                                  sar_stream_t stream) {
+    RankPtrs p;
+    bool vec = false, launch = false;
+    sar_status st = check_rsag(nullptr, out, nranks, count, dtype, false, &p, &vec, &launch);
+    if (st != SAR_OK || !launch) return st;
+    return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), rsag_chunk(count, nranks, dtype), vec,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API size_t sar_ll_packet_bytes(size_t count, sar_dtype dtype) {
+    if (!valid_dtype(dtype)) return 0;
+    const size_t es = esize_of(dtype);
+    if (!count_fits(count, es)) return 0;
+    return (count * es + 3) / 4 * 8;
+}
+
+SAR_API sar_status sar_ll_pack(const void* const* in, void* const* pkts, int nranks, size_t count,
+                               sar_dtype dtype, uint32_t epoch, sar_stream_t stream) {
+    bool launch = false, in16 = false;
+    sar_status st = check_ll(in, pkts, nranks, count, dtype, epoch, &launch, &in16);
+    if (st != SAR_OK || !launch) return st;
+    RankPtrs p;
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < nranks; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = pkts[r];
+    }
+    return to_status(launch_ll_pack(nranks, p, count * esize_of(dtype), epoch, in16,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API sar_status sar_ll_unpack_reduce(const void* const* pkts, void* const* out, int nranks, size_t count,
+                                        sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                                        int32_t* d_status, sar_stream_t stream) {
+    bool launch = false, out16 = false;
+    sar_status st = check_ll(out, pkts, nranks, count, dtype, epoch, &launch, &out16);
+    if (st != SAR_OK) return st;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (!launch) return SAR_OK;
+    RankPtrs p;
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < nranks; ++r) {
+        p.in[r] = pkts[r];
+        p.out[r] = out[r];
+    }
+    return to_status(launch_ll_unpack_reduce(dtype, nranks, p, count, epoch, max_spins, d_status, out16,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                                    size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                                    int32_t* d_status, sar_stream_t stream) {
+    bool launch = false, in16 = false, out16 = false;
+    sar_status st = check_ll(in, pkts, nranks, count, dtype, epoch, &launch, &in16);
+    if (st != SAR_OK) return st;
+    if (out == nullptr) return SAR_ERR_INVALID_ARG;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (!launch) return SAR_OK;
+    if ((st = check_ll(out, pkts, nranks, count, dtype, epoch, &launch, &out16)) != SAR_OK) return st;
+    RankPtrs pack, unpack;
+    std::memset(&pack, 0, sizeof(pack));
+    std::memset(&unpack, 0, sizeof(unpack));
+    for (int r = 0; r < nranks; ++r) {
+        pack.in[r] = in[r];
+        pack.out[r] = pkts[r];
+        unpack.in[r] = pkts[r];
+        unpack.out[r] = out[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = to_status(launch_ll_pack(nranks, pack, count * esize_of(dtype), epoch, in16, s));
+    if (st != SAR_OK) return st;
+    return to_status(launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, s));
+}
+
+SAR_API sar_status sar_fp8_convert(const void* src, sar_dtype src_dtype, void* dst, sar_dtype dst_dtype,
+                                   size_t count, sar_stream_t stream) {
+    if (!valid_dtype(src_dtype) || !valid_dtype(dst_dtype)) return SAR_ERR_UNSUPPORTED_DTYPE;
+    const bool pair_ok = (src_dtype == SAR_FP8_E4M3FN) != (dst_dtype == SAR_FP8_E4M3FN);
+    if (!pair_ok) return SAR_ERR_UNSUPPORTED_DTYPE;
+    if (src == nullptr || dst == nullptr) return SAR_ERR_INVALID_ARG;
+    const size_t ses = esize_of(src_dtype), des = esize_of(dst_dtype);
+    if (!count_fits(count, 4)) return SAR_ERR_INVALID_ARG;
+    if (!aligned(src, ses) || !aligned(dst, des)) return SAR_ERR_MISALIGNED;
+    if (count == 0) return SAR_OK;
+    const bool vec = aligned(src, 16) && aligned(dst, 16);
+    return to_status(launch_convert(src, src_dtype, dst, dst_dtype, count, vec,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API sar_status sar_read_device_status(const int32_t* d_status, sar_stream_t stream) {
+    if (d_status == nullptr) return SAR_ERR_INVALID_ARG;
+    int32_t h = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&h, d_status, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SAR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SAR_ERR_CUDA;
+    if (h == 0) return SAR_OK;
+    if (h == SAR_ERR_TIMEOUT) return SAR_ERR_TIMEOUT;
+    return SAR_ERR_CUDA;
+}
+
+SAR_API const char* sar_status_string(sar_status status) {
+    switch (status) {
+    case SAR_OK: return "SAR_OK";
+    case SAR_ERR_INVALID_ARG: return "SAR_ERR_INVALID_ARG: invalid argument";
+    case SAR_ERR_UNSUPPORTED_NRANKS: return "SAR_ERR_UNSUPPORTED_NRANKS: nranks must be 1, 2, 4, 8, 16 or 32";
+    case SAR_ERR_UNSUPPORTED_DTYPE: return "SAR_ERR_UNSUPPORTED_DTYPE: unsupported element type or conversion";
+    case SAR_ERR_MISALIGNED: return "SAR_ERR_MISALIGNED: buffer not aligned to its element (packets: 16 bytes)";
+    case SAR_ERR_CUDA: return "SAR_ERR_CUDA: a CUDA launch or copy failed";
+    case SAR_ERR_TIMEOUT: return "SAR_ERR_TIMEOUT: an LL flag poll ran out of spins";
+    }
+    return "unknown sar_status";
+}
+
+}  // extern "C"

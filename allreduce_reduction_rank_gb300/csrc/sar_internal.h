@@ -1,0 +1,46 @@
+// sar_internal.h -- launchers between the C ABI (sar_api.cu) and the kernels.
+// All arguments have been validated by the caller.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/sar.h"
+
+namespace sar {
+
+// What an rsag launch writes: the fused allreduce writes the reduced chunk to
+// every output; the reduce-scatter step writes it to the owning rank only.
+enum RsagMode { kFused = 0, kReduceScatter = 1 };
+
+struct RankPtrs {
+    const void* in[SAR_MAX_RANKS];
+    void* out[SAR_MAX_RANKS];
+};
+
+// rsag reduce (fused or reduce-scatter).  `vec` selects 16-byte vectors
+// (every buffer 16-byte aligned).
+cudaError_t launch_rsag(RsagMode mode, sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
+                        size_t chunk, bool vec, cudaStream_t stream);
+
+// rsag all-gather: out[j][chunk r] = out[r][chunk r], j != r (bytes).
+cudaError_t launch_all_gather(int nranks, const RankPtrs& p, size_t count, size_t esize,
+                              size_t chunk, bool vec, cudaStream_t stream);
+
+// LL pack: pkts[r] <- packets of in[r] (p.out holds the packet buffers).
+cudaError_t launch_ll_pack(int nranks, const RankPtrs& p, size_t bytes, uint32_t epoch,
+                           bool vec, cudaStream_t stream);
+
+// LL poll + unpack + reduce + write-back (p.in holds the packet buffers).
+cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
+                                    uint32_t epoch, uint64_t max_spins, int32_t* status,
+                                    bool vec_out, cudaStream_t stream);
+
+cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
+                           size_t count, bool vec, cudaStream_t stream);
+
+size_t esize_of(sar_dtype dt);
+
+}  // namespace sar

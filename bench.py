@@ -1,0 +1,460 @@
+"""Benchmark of libsar on one GB300 (or N replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+
+Workload (a "step"): one sar_allreduce, rsag style, over 8 simulated ranks of
+32M fp16 elements (64 MiB) each, values N(0,1) from seed 1 -- reduce every
+rank chunk in binary32 in rank order, round once, write to all 8 outputs.
+Bytes counted per step: N*S read + N*S written = 1 GiB (GB = 1e9 below).
+The working set (1 GiB) is far larger than the 129 MB L2, so no flush is
+needed between steps.
+
+Printed: one JSON line.  `value` is whole-job HBM GB/s over all GPUs (each GPU
+runs the same workload on its own buffers: replicas, weak scaling), `e2e`
+the same metric through the C ABI with the inputs copied in from pinned host
+memory and all outputs copied back inside the timed region, `roofline` the
+dominant kernel's achieved bandwidth against the measured copy peak, `rows`
+the other workloads (eager and CUDA-graph µs/call and GB/s), and
+`cpu_baseline` the CPU oracle timed on a sample of the same workload.
+
+--impl reference times the CPU oracle itself on a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+GB = 1e9
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic of one launch of the dominant kernel (rsag fused, fp16, 8 ranks,
+# 64 MiB per rank) from one ncu capture, valid while the kernel sources hash to
+# `sources_sha`; otherwise `traffic` is reported as null.
+TRAFFIC = {"sources_sha": None, "bytes_per_launch": None}
+KERNEL_SOURCES = ["allreduce_reduction_rank_gb300/csrc/rsag.cu",
+                  "allreduce_reduction_rank_gb300/csrc/sar_device.cuh"]
+
+
+def sources_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (host-side only: barrier and max over ranks).
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": inside[0][2],
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm.
+# ---------------------------------------------------------------------------
+TORCH_STORAGE = {"bf16": "int16", "fp16": "int16", "fp32": "float32", "e4m3fn": "uint8"}
+NP_VIEW = {"bf16": np.int16, "fp16": np.int16, "fp32": np.float32, "e4m3fn": np.uint8}
+
+
+def upload(torch, codes, dt, dev):
+    return torch.from_numpy(np.ascontiguousarray(codes).view(NP_VIEW[dt])).to(dev)
+
+
+def time_calls(torch, fn, calls: int, stream) -> float:
+    """Average ms per call of `calls` back-to-back calls, CUDA events on `stream`."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(calls):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / calls
+
+
+def time_graph(torch, fn, calls: int, stream) -> float:
+    """Average ms per call with `calls` calls captured into one CUDA graph."""
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(calls):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / calls
+
+
+def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, graph=True, ins=None):
+    ins = ins if ins is not None else wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    pi, po = [t.data_ptr() for t in din], [t.data_ptr() for t in dout]
+
+    def call():
+        sar.sar_allreduce(pi, po, count=wl.count, dtype=wl.dtype, algo=algo, stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            call()
+        eager = time_calls(torch, call, calls, stream)
+        g = time_graph(torch, call, calls, stream) if graph else None
+    row = {"workload": wl.name, "algo": ["rsag", "rsag_two_phase"][algo], "bytes": wl.algo_bytes,
+           "eager_us": round(eager * 1e3, 3), "eager_GBps": round(wl.algo_bytes / (eager * 1e-3) / GB, 1),
+           "l2_resident": wl.algo_bytes <= l2_bytes}
+    if g is not None:
+        row["graph_us"] = round(g * 1e3, 3)
+        row["graph_GBps"] = round(wl.algo_bytes / (g * 1e-3) / GB, 1)
+    del din, dout
+    return row
+
+
+def ll_row(torch, sar, wl, dev, stream, calls):
+    ins = wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    pk = [torch.zeros(sar.sar_ll_packet_bytes(wl.count, wl.dtype), dtype=torch.uint8, device=dev)
+          for _ in range(wl.nranks)]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pi, po, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in dout], [t.data_ptr() for t in pk]
+    epoch = [0]
+
+    def call():
+        epoch[0] += 1
+        sar.sar_allreduce_ll(pi, po, pp, epoch[0], st.data_ptr(), count=wl.count, dtype=wl.dtype,
+                             stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_calls(torch, call, calls, stream)
+    ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    phys = 6 * wl.nranks * wl.bytes_per_rank
+    return {"workload": wl.name, "calls": calls, "epochs": f"1..{calls}", "us_per_call": round(ms * 1e3, 3),
+            "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
+            "physical_GBps": round(phys / (ms * 1e-3) / GB, 2), "status_ok": ok}
+
+
+def convert_row(torch, sar, dev, stream, count=1 << 26):
+    x = torch.randn(count, dtype=torch.float32, device=dev, generator=torch.Generator(device=dev).manual_seed(0))
+    y = torch.empty(count, dtype=torch.uint8, device=dev)
+    z = torch.empty(count, dtype=torch.float32, device=dev)
+
+    def down():
+        sar.sar_fp8_convert(x.data_ptr(), y.data_ptr(), src_dtype="fp32", dst_dtype="e4m3fn", count=count,
+                            stream=stream.cuda_stream)
+
+    def up():
+        sar.sar_fp8_convert(y.data_ptr(), z.data_ptr(), src_dtype="e4m3fn", dst_dtype="fp32", count=count,
+                            stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        down(); up()
+        t_down = time_calls(torch, down, 20, stream)
+        t_up = time_calls(torch, up, 20, stream)
+    b = count * 5
+    return {"workload": f"fp8_convert_{count}", "fp32_to_e4m3fn_us": round(t_down * 1e3, 2),
+            "fp32_to_e4m3fn_GBps": round(b / (t_down * 1e-3) / GB, 1),
+            "e4m3fn_to_fp32_us": round(t_up * 1e3, 2), "e4m3fn_to_fp32_GBps": round(b / (t_up * 1e-3) / GB, 1)}
+
+
+def cpu_baseline(ins, wl, budget_s: float = 10.0) -> dict:
+    """The oracle as it stands, single-threaded, on a slice of the workload."""
+    import oracle
+    sample = 1 << 20
+    part = [x[:sample] for x in ins]
+    runs, t_total = [], 0.0
+    while t_total < budget_s or len(runs) < 2:
+        t = time.perf_counter()
+        oracle.allreduce(part, wl.dtype)
+        dt = time.perf_counter() - t
+        runs.append(dt)
+        t_total += dt
+    med = statistics.median(runs)
+    bytes_ = 2 * wl.nranks * sample * W.ESIZE[wl.dtype]
+    return {"value": round(bytes_ / med / GB, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {sample} elements of each of the {wl.nranks} ranks of {wl.name}, "
+                      f"median of {len(runs)} runs ({t_total:.1f} s), same byte convention",
+            "us_per_call_sample": round(med * 1e6, 1), "host_cpus": os.cpu_count()}
+
+
+def run_gpu(args, d: Dist) -> None:
+    import torch
+    import allreduce_reduction_rank_gb300 as sar
+
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    stream = torch.cuda.Stream(device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = getattr(props, "L2_cache_size", 0) or (129 << 20)
+    peak, peak_kind = measured_peaks()
+    wl = W.C2
+
+    ins = wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    pi, po = [t.data_ptr() for t in din], [t.data_ptr() for t in dout]
+
+    def step():
+        sar.sar_allreduce(pi, po, count=wl.count, dtype=wl.dtype, algo=sar.SAR_ALGO_RSAG,
+                          stream=stream.cuda_stream)
+
+    clocks = ClockSampler(d.local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        # keep the GPU busy for a moment so the clock samples see it under load
+        t_settle = time.time()
+        while time.time() - t_settle < 0.5:
+            step()
+            torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        d.barrier()
+    clocks.stop()
+    ms_total = d.max(start.elapsed_time(end))
+    ms_step = ms_total / args.steps
+    value = d.world * wl.algo_bytes * args.steps / (ms_total * 1e-3) / GB
+    kernel_gbs = wl.algo_bytes / (ms_step * 1e-3) / GB      # one launch per step
+
+    # CUDA graph of the same step
+    with torch.cuda.stream(stream):
+        g_ms = time_graph(torch, step, min(args.steps, 50), stream)
+
+    # End to end through the C ABI with host buffers: H2D of all inputs, the
+    # allreduce, D2H of all outputs, every step.
+    h_in = [torch.from_numpy(x.view(NP_VIEW[wl.dtype])).pin_memory() for x in ins]
+    h_out = [torch.empty(wl.count, dtype=din[0].dtype).pin_memory() for _ in range(wl.nranks)]
+
+    def e2e_step():
+        for h, t in zip(h_in, din):
+            t.copy_(h, non_blocking=True)
+        step()
+        for h, t in zip(h_out, dout):
+            h.copy_(t, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        e2e_step()
+        d.barrier()
+        e2e_ms = d.max(time_calls(torch, e2e_step, e2e_steps, stream) * e2e_steps) / e2e_steps
+    e2e_ok = all(torch.equal(h_out[j], h_out[0]) for j in range(wl.nranks))
+    del h_in, h_out
+
+    rows = []
+    if args.rows and d.rank == 0:
+        del din, dout
+        torch.cuda.empty_cache()
+        rows.append(rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=1, ins=ins))
+        rows.append(rsag_row(torch, sar, W.C1, dev, stream, l2_bytes))
+        for w in W.C3:
+            rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes))
+        rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes))
+        for w in W.C5:
+            rows.append(ll_row(torch, sar, w, dev, stream, W.LL_CALLS))
+        rows.append(convert_row(torch, sar, dev, stream))
+
+    cpu = cpu_baseline(ins, wl) if d.rank == 0 and d.world == 1 and args.cpu_baseline else None
+    sha = sources_sha()
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha"] == sha else None
+    clk = clocks.summary(t0 - 0.6, t1)
+    if d.rank == 0:
+        line = {
+            "metric": "simulated-allreduce HBM GB/s (% of GB300 peak) and us/call vs message size",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": d.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_call": round(ms_step * 1e3, 2),
+            "pct_of_peak": round(100 * kernel_gbs / peak, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)",
+            "data": "synthetic (seeded splitmix64, N(0,1))",
+            "config": {"workload": wl.name, "nranks": wl.nranks, "count_per_rank": wl.count,
+                       "bytes_per_rank": wl.bytes_per_rank, "algo": "rsag (fused reduce + write-back)",
+                       "bytes_per_step": wl.algo_bytes, "byte_convention": "N*S read + N*S written",
+                       "l2": "working set 1 GiB > 129 MB L2; no flush between steps",
+                       "parallelism": f"replicas x{d.world} (one independent workload per GPU)"},
+            "graph": {"us_per_call": round(g_ms * 1e3, 2), "GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 1)},
+            "e2e": {"value": round(d.world * wl.algo_bytes / (e2e_ms * 1e-3) / GB, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": wl.nranks * wl.bytes_per_rank,
+                    "d2h_bytes_per_step": wl.nranks * wl.bytes_per_rank, "steps": e2e_steps,
+                    "ms_per_step": round(e2e_ms, 3), "outputs_identical": e2e_ok},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(kernel_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                         "traffic": traffic, "algorithmic_bytes": wl.algo_bytes,
+                         "kernel": "rsag_vec_kernel<fp16, 8, fused>", "kernel_sources_sha": sha},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, d: Dist) -> None:
+    """The CPU oracle as it stands, on a bounded sample of the same workload."""
+    if d.rank != 0:
+        return
+    import oracle
+    wl = W.C2
+    sample = 1 << 19
+    ins = [W.rank_input(wl.dist, wl.seed, wl.dtype, sample, r, wl.sigma) for r in range(wl.nranks)]
+    for _ in range(args.warmup):
+        oracle.allreduce(ins, wl.dtype)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.allreduce(ins, wl.dtype)
+    el = time.perf_counter() - t
+    bytes_ = 2 * wl.nranks * sample * W.ESIZE[wl.dtype]
+    value = bytes_ * args.steps / el / GB
+    line = {"impl": "reference", "metric": "simulated-allreduce HBM GB/s (% of GB300 peak) and us/call vs message size",
+            "value": round(value, 4), "unit": "GB/s", "n_gpus": d.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": wl.name, "nranks": wl.nranks, "count_per_rank": wl.count,
+                       "algo": "rsag (oracle: plain rank-ordered sum)",
+                       "sample": f"first {sample} elements of each rank per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {sample} elements of each of the {wl.nranks} ranks per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", dest="rows", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    d = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, d)
+        else:
+            run_gpu(args, d)
+    finally:
+        d.close()
+
+
+if __name__ == "__main__":
+    main()

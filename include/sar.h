@@ -1,0 +1,220 @@
+/*
+ * sar.h -- libsar, the simulated allreduce on one GB300 (sm_103a).
+ *
+ * N simulated ranks are N separate buffers in the HBM of one GPU.  The library
+ * computes the data-parallel hot path of the MSCCL++ allreduce algorithms: the
+ * N-way elementwise sum of the ranks' buffers, accumulated in binary32 and
+ * rounded once to the element type, in two styles:
+ *
+ *   rsag  - reduce-scatter then all-gather ("Support 2 ranks in
+ *           AllreduceRsAgZeroCopy - #948", sections "why" and "what changed":
+ *           each rank reduces its 1/N chunk of every peer's input and writes
+ *           the result back to every peer's output);
+ *   LL    - all-pair low-latency packets (mscclpp commit history, the
+ *           allreduce_allpair_packet fix: send, reduce and write-back in one
+ *           thread block, with flag-checked packets).
+ *
+ * Accumulation is always binary32 (mscclpp commit history, "Add
+ * mixed-precision accumulation for allreduce": accumDtype), summed in rank
+ * order 0..N-1 for every element and every output, then rounded once with
+ * round-to-nearest-even.  Results are therefore reproducible bit for bit.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointer arrays (`in`, `out`, `pkts`) are HOST arrays of `nranks` DEVICE
+ *    pointers.  The caller owns the arrays and every buffer.  The library
+ *    copies the pointers into kernel parameters, keeps nothing after the call
+ *    returns, allocates nothing and does not synchronise (except
+ *    sar_read_device_status), so calls are stream-ordered and may be captured
+ *    into a CUDA graph.
+ *  - `count` is the number of elements per rank.  count == 0 returns SAR_OK
+ *    without launching anything.
+ *  - Every argument error is returned before any launch.  Supported rank
+ *    counts are 1, 2, 4, 8, 16 and 32; any other count returns
+ *    SAR_ERR_UNSUPPORTED_NRANKS and launches nothing.  (In #948 the rsag
+ *    kernel is instantiated only for 2, 4, 8, 16 and 32 ranks and other
+ *    counts returned an error without launching.)
+ *  - Buffers must be aligned to their element size (else SAR_ERR_MISALIGNED).
+ *    When every buffer of a call is 16-byte aligned the kernels move 16-byte
+ *    vectors; otherwise a slower element-wise kernel runs.  Results are
+ *    identical either way.
+ *  - A failed launch returns SAR_ERR_CUDA.
+ *  - `stream` is a CUDA stream (cudaStream_t); NULL is the legacy default
+ *    stream.  The current device must be the one that owns the buffers.
+ */
+#ifndef SAR_H_
+#define SAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SAR_API __attribute__((visibility("default")))
+#else
+#define SAR_API
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* sar_stream_t;
+
+#define SAR_MAX_RANKS 32
+
+typedef enum {
+    SAR_BF16 = 0,        /* bfloat16, 2 bytes */
+    SAR_FP16 = 1,        /* IEEE binary16, 2 bytes */
+    SAR_FP32 = 2,        /* IEEE binary32, 4 bytes */
+    SAR_FP8_E4M3FN = 3   /* OCP FP8 E4M3 (bias 7, no inf, NaN = S.1111.111,
+                            max +-448; binary32 -> e4m3fn saturates), 1 byte */
+} sar_dtype;
+
+typedef enum {
+    SAR_ALGO_RSAG = 0,            /* one fused kernel: reduce chunk, write to all outputs */
+    SAR_ALGO_RSAG_TWO_PHASE = 1   /* reduce-scatter kernel, then all-gather kernel */
+} sar_algo;
+
+typedef enum {
+    SAR_OK = 0,
+    SAR_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum, epoch 0, size overflow, ... */
+    SAR_ERR_UNSUPPORTED_NRANKS = 2, /* nranks not in {1, 2, 4, 8, 16, 32} */
+    SAR_ERR_UNSUPPORTED_DTYPE = 3,  /* dtype (or conversion pair) not supported */
+    SAR_ERR_MISALIGNED = 4,         /* buffer not aligned to its element size (16 B for packets) */
+    SAR_ERR_CUDA = 5,               /* a CUDA launch or copy failed */
+    SAR_ERR_TIMEOUT = 6             /* an LL flag poll ran out of spins (reported on the device) */
+} sar_status;
+
+/*
+ * sar_allreduce -- the rsag allreduce.
+ *
+ * Defined by "Support 2 ranks in AllreduceRsAgZeroCopy - #948" ("why": the
+ * ncclAllReduce that the rsag zero-copy algorithm serves; "what changed":
+ * NPeers = NRanks - 1, peer loops unrolled at compile time).
+ *
+ * For every element i and every rank j:
+ *   out[j][i] = R( (((f32(in[0][i]) + f32(in[1][i])) + f32(in[2][i])) ... + f32(in[N-1][i])) )
+ * with binary32 additions and one round-to-nearest-even R into `dtype`
+ * (e4m3fn saturates to +-448).
+ *
+ * Simulated rank r owns chunk r = [r*C, min(count, (r+1)*C)) where
+ * C = sar_rsag_chunk(count, nranks, dtype).  SAR_ALGO_RSAG reduces each chunk
+ * and writes it to all N outputs in one kernel (N*S bytes read, N*S written,
+ * S = count * element size).  SAR_ALGO_RSAG_TWO_PHASE runs sar_reduce_scatter
+ * then sar_all_gather.  Both give the same bits.
+ *
+ * in, out : host arrays of `nranks` device pointers, `count` elements each,
+ *           dense.  out[r] == in[r] (in place) is allowed; any other overlap
+ *           between buffers is undefined.
+ */
+SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
+                         sar_dtype dtype, sar_algo algo, sar_stream_t stream);
+
+/*
+ * sar_reduce_scatter -- the rsag reduce step alone.
+ * For every rank r: out[r][chunk r] = the reduced chunk (as in sar_allreduce).
+ * No other element of any output is written.
+ */
+SAR_API sar_status sar_reduce_scatter(const void* const* in, void* const* out, int nranks, size_t count,
+                              sar_dtype dtype, sar_stream_t stream);
+
+/*
+ * sar_all_gather -- the rsag write-back step alone.
+ * For every rank r and every j != r: out[j][chunk r] = out[r][chunk r]
+ * (a bitwise copy).  After sar_reduce_scatter this completes the allreduce.
+ */
+SAR_API sar_status sar_all_gather(void* const* out, int nranks, size_t count, sar_dtype dtype,
+                          sar_stream_t stream);
+
+/*
+ * sar_rsag_chunk -- elements per rank chunk: ceil(count / nranks) rounded up
+ * to a whole 16-byte vector of elements.  Returns 0 for invalid arguments.
+ */
+SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype);
+
+/*
+ * sar_ll_packet_bytes -- bytes of one rank's LL packet buffer:
+ * ceil(count * element size / 4) packets of 8 bytes.  0 for a bad dtype.
+ *
+ * Packet w of rank r (mscclpp commit history, allreduce_allpair_packet fix;
+ * layout: 4-byte payload + 4-byte flag): bytes 0..3 are bytes 4w..4w+3 of
+ * in[r] (zero past the end of the input), bytes 4..7 the epoch as a
+ * little-endian uint32.  Each packet is written with one 8-byte store and read
+ * with one 8-byte load, so a reader that sees the flag also sees the payload.
+ *
+ * Packet buffers belong to the caller, must be 16-byte aligned, and must be
+ * zeroed once before first use: epoch 0 is reserved for "never written"
+ * (mscclpp commit history, the TokenPool fix: recycled counters must not keep
+ * stale values).  Epochs must not repeat while a buffer can still hold packets
+ * of the earlier use; after 2^32 - 1 epochs, zero the buffers again.
+ */
+SAR_API size_t sar_ll_packet_bytes(size_t count, sar_dtype dtype);
+
+/*
+ * sar_ll_pack -- the LL send: rank r's whole input is written as packets to
+ * pkts[r], every flag = epoch.  epoch == 0 returns SAR_ERR_INVALID_ARG.
+ */
+SAR_API sar_status sar_ll_pack(const void* const* in, void* const* pkts, int nranks, size_t count,
+                       sar_dtype dtype, uint32_t epoch, sar_stream_t stream);
+
+/*
+ * sar_ll_unpack_reduce -- the LL reduce and write-back.
+ *
+ * Simulated rank r owns a 1/N chunk of the packet index range (whole groups of
+ * 4 packets).  For each packet in it, for k = 0..N-1 in order, it loads
+ * pkts[k]'s packet, polls until the flag equals `epoch`, adds the payload's
+ * elements in binary32, rounds once and stores the elements to all N outputs.
+ * The values equal sar_allreduce's.
+ *
+ * A poll re-reads a packet at most `max_spins` times (with a short sleep
+ * between reads).  When one runs out, the kernel stores SAR_ERR_TIMEOUT into
+ * *d_status (only if it still holds 0), every thread stops polling, and the
+ * outputs are unspecified; the call itself has already returned SAR_OK.
+ * Read the status with sar_read_device_status.
+ *
+ * d_status : caller-owned device int32, zeroed by the caller; it is never
+ *            cleared by the library, so one word can collect the status of
+ *            many calls.  max_spins == 0 returns SAR_ERR_INVALID_ARG.
+ */
+SAR_API sar_status sar_ll_unpack_reduce(const void* const* pkts, void* const* out, int nranks, size_t count,
+                                sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                                int32_t* d_status, sar_stream_t stream);
+
+/*
+ * sar_allreduce_ll -- the LL all-pair allreduce: sar_ll_pack then
+ * sar_ll_unpack_reduce with the same epoch, stream-ordered.  `pkts` is the
+ * caller's packet scratch (nranks buffers of sar_ll_packet_bytes each).
+ */
+SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                            size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                            int32_t* d_status, sar_stream_t stream);
+
+/*
+ * sar_fp8_convert -- dst[i] = R_dst(f32(src[i])) for count elements.
+ *
+ * Supported pairs: e4m3fn -> {fp32, fp16, bf16} (exact) and
+ * {fp32, fp16, bf16} -> e4m3fn (one round-to-nearest-even, finite overflow and
+ * infinities saturate to +-448, NaN stays NaN).  FP8 with higher-precision
+ * accumulation: mscclpp commit history, the ROCm FP8 summary and "Add
+ * mixed-precision accumulation for allreduce".  Other pairs return
+ * SAR_ERR_UNSUPPORTED_DTYPE.  src and dst must not overlap.
+ */
+SAR_API sar_status sar_fp8_convert(const void* src, sar_dtype src_dtype, void* dst, sar_dtype dst_dtype,
+                           size_t count, sar_stream_t stream);
+
+/*
+ * sar_read_device_status -- synchronises `stream`, reads *d_status and returns
+ * it as a sar_status (SAR_OK or SAR_ERR_TIMEOUT), or SAR_ERR_CUDA if the copy
+ * fails.  Not for use inside a CUDA graph capture.
+ */
+SAR_API sar_status sar_read_device_status(const int32_t* d_status, sar_stream_t stream);
+
+/* sar_status_string -- a static, human-readable name for a status. */
+SAR_API const char* sar_status_string(sar_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAR_H_ */

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point that include/sar.h declares, and its host-side argument checks return
+the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sar.h")
+
+
+@pytest.fixture(scope="module")
+def sar():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_sar_build", os.path.join(ROOT, "allreduce_reduction_rank_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import allreduce_reduction_rank_gb300 as s
+    return s
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"SAR_API\s+[\w\s\*]+?\b(sar_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("sar_allreduce", "sar_ll_pack", "sar_ll_unpack_reduce", "sar_fp8_convert",
+                 "sar_ll_packet_bytes", "sar_read_device_status", "sar_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(sar):
+    lib = ctypes.CDLL(sar.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sar.h but not exported"
+
+
+def test_only_declared_symbols_are_exported(sar):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", sar.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm unavailable")
+    exported = sorted({ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln})
+    assert exported == declared_functions()
+
+
+def test_status_strings(sar):
+    for st in range(7):
+        assert sar.sar_status_string(st).startswith("SAR_")
+    assert "unknown" in sar.sar_status_string(99)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn"])
+def test_chunk_rule_matches_oracle(sar, dt):
+    for count in (0, 1, 7, 9, 4097, 1 << 20, (1 << 25) + 3):
+        for n in (1, 2, 4, 8, 16, 32):
+            c = sar.sar_rsag_chunk(count, n, dt)
+            b, e = oracle.rsag_chunk(count, n, dt, 1 if n > 1 else 0)
+            if n > 1 and b < count:
+                assert b == c
+            assert all(oracle.rsag_chunk(count, n, dt, r)[0] == min(count, r * c) for r in range(n))
+    assert sar.sar_rsag_chunk(10, 3, dt) == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn"])
+def test_packet_bytes_match_oracle(sar, dt):
+    for count in (0, 1, 2, 3, 5, 1000, 262144):
+        assert sar.sar_ll_packet_bytes(count, dt) == 8 * oracle.ll_packets(count, dt)
+    assert sar.lib.sar_ll_packet_bytes(4, 7) == 0
+
+
+def _arr(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def test_argument_errors_before_launch(sar):
+    L = sar.lib
+    ptrs2 = _arr([4096, 8192])
+    # unsupported rank counts (the #948 set plus 1)
+    for n in (0, 3, 5, 6, 7, 9, 33, -1):
+        assert L.sar_allreduce(ptrs2, ptrs2, n, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
+        assert L.sar_ll_pack(ptrs2, ptrs2, n, 16, sar.SAR_BF16, 1, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce(ptrs2, ptrs2, 2, 16, 4, 0, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_allreduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 7, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce(None, ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce(_arr([4096, 0]), ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce(_arr([4096, 4097]), ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce(_arr([4096, 4098]), ptrs2, 2, 16, sar.SAR_FP32, 0, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce(ptrs2, ptrs2, 2, 2 ** 62, sar.SAR_FP32, 0, None) == sar.SAR_ERR_INVALID_ARG
+    # count == 0: nothing to do, nothing launched
+    assert L.sar_allreduce(ptrs2, ptrs2, 2, 0, sar.SAR_BF16, 0, None) == sar.SAR_OK
+    assert L.sar_reduce_scatter(ptrs2, ptrs2, 2, 0, sar.SAR_BF16, None) == sar.SAR_OK
+    assert L.sar_all_gather(ptrs2, 2, 0, sar.SAR_BF16, None) == sar.SAR_OK
+    # LL: epoch 0 is reserved, packets must be 16-byte aligned, status required
+    assert L.sar_ll_pack(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_ll_pack(ptrs2, _arr([4096, 8200]), 2, 16, sar.SAR_BF16, 1, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 100, None, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 0, 4096, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4098, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce_ll(ptrs2, ptrs2, ptrs2, 3, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
+        sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce_ll(ptrs2, None, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4096, None) == sar.SAR_ERR_INVALID_ARG
+    # conversion pairs
+    assert L.sar_fp8_convert(4096, sar.SAR_FP32, 8192, sar.SAR_BF16, 16, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_fp8_convert(4096, sar.SAR_FP8_E4M3FN, 8192, sar.SAR_FP8_E4M3FN, 16, None) == \
+        sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_fp8_convert(4097, sar.SAR_FP32, 8192, sar.SAR_FP8_E4M3FN, 16, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_fp8_convert(None, sar.SAR_FP32, 8192, sar.SAR_FP8_E4M3FN, 16, None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_fp8_convert(4096, sar.SAR_FP32, 8192, sar.SAR_FP8_E4M3FN, 0, None) == sar.SAR_OK
+    assert L.sar_read_device_status(None, None) == sar.SAR_ERR_INVALID_ARG
+
+
+def test_binding_raises_on_error(sar):
+    with pytest.raises(sar.SarError) as ei:
+        sar.sar_allreduce([4096] * 3, [8192] * 3, count=16, dtype="bf16", stream=0)
+    assert ei.value.status == sar.SAR_ERR_UNSUPPORTED_NRANKS

@@ -1,0 +1,220 @@
+"""GPU parity of the rsag allreduce (fused and two-phase) and of its two
+steps, against the CPU oracle, through the C ABI.
+
+Bar: bit-exact (fixed rank order, binary32 accumulation, one rounding), NaN
+compared by class.  Every case also checks the canary bytes around every
+buffer and that the inputs are unchanged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.gpu_util import ESIZE, Guarded, assert_same, random_codes
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["bf16", "fp16", "fp32", "e4m3fn"]
+RANKS = [1, 2, 4, 8, 16, 32]
+
+
+@pytest.fixture(scope="module")
+def sar():
+    import allreduce_reduction_rank_gb300 as s
+    return s
+
+
+def _run(sar, ins, dt, algo, offsets=None, inplace=False):
+    n, count = len(ins), ins[0].size
+    offs = offsets or [0] * n
+    gin = [Guarded.from_codes(c, o) for c, o in zip(ins, offs)]
+    gout = gin if inplace else [Guarded(count * ESIZE[dt], o, fill=0x5A) for o in offs]
+    sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout], count=count, dtype=dt, algo=algo)
+    torch.cuda.synchronize()
+    return gin, gout
+
+
+def _check(gin, gout, ins, want, dt, inplace=False):
+    for j, g in enumerate(gout):
+        assert_same(g.codes(dt), want, dt, f"out[{j}]")
+        assert g.guards_intact(), f"canary overwritten around out[{j}]"
+    if not inplace:
+        for r, g in enumerate(gin):
+            assert_same(g.codes(dt), ins[r], dt, f"in[{r}] modified")
+            assert g.guards_intact()
+
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("count", [1, 7, 9, 17, 4097, 100003])
+@pytest.mark.parametrize("n", RANKS)
+@pytest.mark.parametrize("dt", DTYPES)
+def test_allreduce_matches_oracle(sar, dt, n, count, algo):
+    rng = np.random.default_rng([DTYPES.index(dt), n, count, algo])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, algo)
+    _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_many_tiles_and_ragged_tail(sar, dt, algo):
+    """Several tiles per rank chunk plus a partial last vector."""
+    count = (1 << 21) + 13
+    ins = W.rank_inputs("normal", 5, dt, count, 8, 4.0 if dt == "e4m3fn" else 1.0)
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, algo)
+    _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("n", [2, 8, 32])
+def test_unaligned_buffers_take_the_element_path(sar, dt, n):
+    rng = np.random.default_rng(n)
+    count = 3001
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    offs = [ESIZE[dt] * (r % 3) for r in range(n)]
+    for algo in (0, 1):
+        gin, gout = _run(sar, ins, dt, algo, offsets=offs)
+        _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_in_place(sar, dt, algo):
+    rng = np.random.default_rng(3)
+    ins = [random_codes(rng, dt, 50001) for _ in range(4)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, algo, inplace=True)
+    _check(gin, gout, ins, want, dt, inplace=True)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_nan_and_infinity_inputs(sar, dt):
+    rng = np.random.default_rng(11)
+    ins = [random_codes(rng, dt, 20000, nan_ok=True) for _ in range(4)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, 0)
+    _check(gin, gout, ins, want, dt)
+
+
+def test_rank_order_is_fixed(sar):
+    """In binary32 ((2^24 + 1) - 2^24) + 1 = 1, while any other grouping or
+    the reversed order gives 2."""
+    ins = [np.full(37, v, np.float32) for v in (2.0 ** 24, 1.0, -(2.0 ** 24), 1.0)]
+    for algo in (0, 1):
+        _, gout = _run(sar, ins, "fp32", algo)
+        for g in gout:
+            assert np.all(g.codes("fp32") == 1.0)
+
+
+NEG_ZERO = {"bf16": 0x8000, "fp16": 0x8000, "e4m3fn": 0x80}
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_single_rank_is_identity_including_negative_zero(sar, dt):
+    rng = np.random.default_rng(2)
+    x = random_codes(rng, dt, 10007)
+    if dt == "fp32":
+        x[:2] = np.array([-0.0, 0.0], np.float32)
+    else:
+        x[:2] = np.array([NEG_ZERO[dt], 0]).astype(x.dtype)
+    for algo in (0, 1):
+        _, gout = _run(sar, [x], dt, algo)
+        assert np.array_equal(gout[0].bytes(), x.view(np.uint8))
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("n", [2, 4, 8, 32])
+def test_reduce_scatter_then_all_gather(sar, dt, n):
+    rng = np.random.default_rng(n + 7)
+    count = 20011
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin = [Guarded.from_codes(c) for c in ins]
+    pattern = np.full(count * ESIZE[dt], 0x3C, np.uint8)
+    gout = [Guarded.from_codes(pattern) for _ in range(n)]
+    sar.sar_reduce_scatter([g.ptr for g in gin], [g.ptr for g in gout], count=count, dtype=dt)
+    torch.cuda.synchronize()
+    for r, g in enumerate(gout):
+        b, e = oracle.rsag_chunk(count, n, dt, r)
+        assert sar.sar_rsag_chunk(count, n, dt) * r == b or b == count
+        got = g.bytes()
+        es = ESIZE[dt]
+        assert_same(got[b * es: e * es].view(want.dtype), want[b:e], dt, f"chunk {r}")
+        assert np.all(got[: b * es] == 0x3C) and np.all(got[e * es:] == 0x3C), "wrote outside own chunk"
+        assert g.guards_intact()
+    sar.sar_all_gather([g.ptr for g in gout], count=count, dtype=dt)
+    torch.cuda.synchronize()
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+        assert g.guards_intact()
+
+
+def test_graph_capture_and_replay(sar):
+    dt, n, count = "bf16", 8, 300007
+    rng = np.random.default_rng(9)
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin = [Guarded.from_codes(c) for c in ins]
+    gout = [Guarded(count * 2) for _ in range(n)]
+    gout2 = [Guarded(count * 2) for _ in range(n)]
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout], count=count, dtype=dt, algo=0)
+        sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout2], count=count, dtype=dt, algo=1)
+        with pytest.raises(sar.SarError):       # rejected before launch, capture unaffected
+            sar.sar_allreduce([g.ptr for g in gin[:3]], [g.ptr for g in gout[:3]], count=count, dtype=dt)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for g in gout + gout2:
+        assert_same(g.codes(dt), want, dt)
+        assert g.guards_intact()
+
+
+# ---------------------------------------------------------------------------
+# The measured workloads at full size, in the launch configuration the
+# benchmark times: sampled elements against the oracle, plus the property
+# that every output is identical.
+# ---------------------------------------------------------------------------
+
+def _sample_indices(count, n, dt, rng):
+    idx = [rng.integers(0, count, 100000), np.arange(64), np.arange(count - 64, count)]
+    for r in range(n):
+        b, e = oracle.rsag_chunk(count, n, dt, r)
+        idx.append(np.clip(np.arange(b - 3, b + 3), 0, count - 1))
+    return np.unique(np.concatenate(idx))
+
+
+FULL = [W.C1, W.C2, W.C3[-1], W.C4, W.C4_STRESS]
+
+
+@pytest.mark.parametrize("wl", FULL, ids=[w.name for w in FULL])
+def test_full_size_workload_sampled(sar, wl):
+    dt, n, count = wl.dtype, wl.nranks, wl.count
+    ins = wl.inputs()
+    tdt = {"bf16": torch.int16, "fp16": torch.int16, "fp32": torch.int32, "e4m3fn": torch.uint8}[dt]
+    din = [torch.from_numpy(x.view(np.int16) if ESIZE[dt] == 2 else x.view(np.int32) if dt == "fp32" else x)
+           .cuda() for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(n)]
+    algos = [0, 1] if wl is W.C2 else [0]
+    rng = np.random.default_rng(count)
+    idx = _sample_indices(count, n, dt, rng)
+    sampled = [x[idx] for x in ins]
+    want = oracle.allreduce(sampled, dt)[0]
+    tidx = torch.from_numpy(idx.astype(np.int64)).cuda()
+    for algo in algos:
+        for o in dout:
+            o.fill_(0)
+        sar.sar_allreduce([t.data_ptr() for t in din], [t.data_ptr() for t in dout], count=count, dtype=dt,
+                          algo=algo)
+        torch.cuda.synchronize()
+        for j in range(n):
+            got = dout[j][tidx].cpu().numpy()
+            assert_same(got.view(want.dtype), want, dt, f"{wl.name} out[{j}] sampled")
+            assert torch.equal(dout[j], dout[0]), f"{wl.name}: out[{j}] differs from out[0]"
+        assert tdt == din[0].dtype
