@@ -297,7 +297,7 @@ def run_gpu(args, d: Dist) -> None:
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = getattr(props, "L2_cache_size", 0) or (129 << 20)
     peak, peak_kind = measured_peaks()
-    wl = W.C2
+    wl = WORKLOADS[args.workload]
 
     ins = wl.inputs()
     din = [upload(torch, x, wl.dtype, dev) for x in ins]
@@ -315,7 +315,7 @@ def run_gpu(args, d: Dist) -> None:
             step()
         # keep the GPU busy for a moment so the clock samples see it under load
         t_settle = time.time()
-        while time.time() - t_settle < 0.5:
+        while time.time() - t_settle < args.settle_s:
             step()
             torch.cuda.synchronize()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -360,7 +360,7 @@ def run_gpu(args, d: Dist) -> None:
     del h_in, h_out
 
     rows = []
-    if args.rows and d.rank == 0:
+    if args.rows and d.rank == 0 and wl is W.C2:
         del din, dout
         torch.cuda.empty_cache()
         rows.append(rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=1, ins=ins))
@@ -375,19 +375,22 @@ def run_gpu(args, d: Dist) -> None:
     cpu = cpu_baseline(ins, wl) if d.rank == 0 and d.world == 1 and args.cpu_baseline else None
     sha = sources_sha()
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha"] == sha else None
-    clk = clocks.summary(t0 - 0.6, t1)
+    clk = clocks.summary(t0 - args.settle_s - 0.1, t1)
     if d.rank == 0:
         line = {
             "metric": "simulated-allreduce HBM GB/s (% of GB300 peak) and us/call vs message size",
             "value": round(value, 1), "unit": "GB/s", "n_gpus": d.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_call": round(ms_step * 1e3, 2),
             "pct_of_peak": round(100 * kernel_gbs / peak, 1),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)",
-            "data": "synthetic (seeded splitmix64, N(0,1))",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": f"{wl.dtype} (fp32 accumulate)",
+            "data": f"synthetic (seeded splitmix64, {wl.dist}, seed {wl.seed})",
             "config": {"workload": wl.name, "nranks": wl.nranks, "count_per_rank": wl.count,
                        "bytes_per_rank": wl.bytes_per_rank, "algo": "rsag (fused reduce + write-back)",
                        "bytes_per_step": wl.algo_bytes, "byte_convention": "N*S read + N*S written",
-                       "l2": "working set 1 GiB > 129 MB L2; no flush between steps",
+                       "l2": (f"working set {wl.algo_bytes / 2**20:.0f} MiB vs {l2_bytes / 2**20:.0f} MiB L2; "
+                              + ("larger than L2, no flush between steps" if wl.algo_bytes > l2_bytes
+                                 else "L2-resident (fraction of HBM peak not meaningful)")),
                        "parallelism": f"replicas x{d.world} (one independent workload per GPU)"},
             "graph": {"us_per_call": round(g_ms * 1e3, 2), "GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 1)},
             "e2e": {"value": round(d.world * wl.algo_bytes / (e2e_ms * 1e-3) / GB, 2), "unit": "GB/s",
@@ -398,7 +401,7 @@ def run_gpu(args, d: Dist) -> None:
             "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(kernel_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": traffic, "algorithmic_bytes": wl.algo_bytes,
-                         "kernel": "rsag_vec_kernel<fp16, 8, fused>", "kernel_sources_sha": sha},
+                         "kernel": f"rsag_vec_kernel<{wl.dtype}, {wl.nranks}, fused>", "kernel_sources_sha": sha},
             "clocks": clk,
             "cpu_baseline": cpu,
             "rows": rows,
@@ -435,8 +438,15 @@ def run_reference(args, d: Dist) -> None:
     print(json.dumps(line), flush=True)
 
 
+WORKLOADS = {w.name: w for w in [W.C1, W.C2, W.C4, W.C4_STRESS] + W.C3}
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=W.C2.name,
+                    help="rsag workload timed as the step (default: the 8x64MiB fp16 headline)")
+    ap.add_argument("--settle-s", type=float, default=0.5,
+                    help="seconds of untimed calls before the timed region (clock samples under load)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
