@@ -74,6 +74,7 @@ def _bind(lib):
     lib.orc_decode_array.argtypes, lib.orc_decode_array.restype = [i32, vp, vp, sz], None
     lib.orc_add_f32.argtypes, lib.orc_add_f32.restype = [ctypes.c_float, ctypes.c_float], ctypes.c_float
     lib.orc_allreduce.argtypes, lib.orc_allreduce.restype = [vpp, vpp, i32, sz, i32], i32
+    lib.orc_allreduce_accum.argtypes, lib.orc_allreduce_accum.restype = [vpp, vpp, i32, sz, i32, i32], i32
     lib.orc_reduce_scatter.argtypes, lib.orc_reduce_scatter.restype = [vpp, vpp, i32, sz, i32], i32
     lib.orc_all_gather.argtypes, lib.orc_all_gather.restype = [vpp, i32, sz, i32], i32
     lib.orc_rsag_chunk.argtypes = [sz, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
@@ -163,6 +164,19 @@ def allreduce(ins, dtype) -> list:
     rc = _load().orc_allreduce(_ptrs(ins), _ptrs(outs), len(ins), count, dt)
     if rc != OK:
         raise ValueError(f"oracle allreduce rejected arguments ({rc})")
+    return outs
+
+
+def allreduce_accum(ins, dtype, accum) -> list:
+    """Every partial sum rounded into `accum` (native when accum == dtype)."""
+    dt, at = _dt(dtype), _dt(accum)
+    ins = [np.ascontiguousarray(a) for a in ins]
+    count = ins[0].size
+    _check_ranks(ins, count, dt)
+    outs = [np.empty(count, dtype=NP_STORAGE[dt]) for _ in ins]
+    rc = _load().orc_allreduce_accum(_ptrs(ins), _ptrs(outs), len(ins), count, dt, at)
+    if rc != OK:
+        raise ValueError(f"oracle allreduce_accum rejected arguments ({rc})")
     return outs
 
 

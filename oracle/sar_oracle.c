@@ -290,6 +290,32 @@ int orc_allreduce(const void* const* in, void* const* out, int nranks,
     return ORC_OK;
 }
 
+/* Accumulation in another type (mscclpp commit history, "Add mixed-precision
+ * accumulation for allreduce": accumDtype, with AUTO resolving to the input
+ * type, and FP8 inputs reduced in float16 or float32).  Every partial sum is
+ * rounded into the accumulator type:
+ *     acc_0 = R_acc(f32(in[0][i]))
+ *     acc_k = R_acc(f32(acc_{k-1}) + f32(in[k][i]))      (binary32 add, RNE)
+ *     out[j][i] = R_dt(f32(acc_{N-1}))
+ * acc_dt == ORC_FP32 is orc_allreduce; acc_dt == dt is native accumulation. */
+static float round_through(int acc_dt, float x) {
+    uint8_t tmp[4];
+    orc_store(acc_dt, tmp, 0, x);
+    return orc_load(acc_dt, tmp, 0);
+}
+
+int orc_allreduce_accum(const void* const* in, void* const* out, int nranks,
+                        size_t count, int dt, int acc_dt) {
+    if (!valid_args(nranks, dt) || orc_esize(acc_dt) == 0) return ORC_BAD_ARG;
+    for (size_t i = 0; i < count; ++i) {
+        float acc = round_through(acc_dt, orc_load(dt, in[0], i));
+        for (int k = 1; k < nranks; ++k)
+            acc = round_through(acc_dt, acc + orc_load(dt, in[k], i));
+        for (int j = 0; j < nranks; ++j) orc_store(dt, out[j], i, acc);
+    }
+    return ORC_OK;
+}
+
 /* Chunk of simulated rank r: C = ceil(count / N) rounded up to a multiple of
  * the elements in 16 bytes; chunk r = [r*C, min(count, (r+1)*C)), possibly
  * empty. */

@@ -10,6 +10,7 @@ import os
 import pytest
 
 import oracle
+from tests import test_oracle_accum as ta
 from tests import test_oracle_formats as tf
 from tests import test_oracle_sum as ts
 
@@ -47,6 +48,12 @@ MUTANTS = {
         ("at < bytes ? src[at] : 0;", "at < bytes ? src[at] : 0xFF;"),
     "chunk not rounded to a vector":
         ("    c = (c + vec - 1) / vec * vec;\n", ""),
+    "partial sums not rounded into the accumulator":
+        ("            acc = round_through(acc_dt, acc + orc_load(dt, in[k], i));",
+         "            acc = acc + orc_load(dt, in[k], i);"),
+    "accumulator seed not rounded":
+        ("        float acc = round_through(acc_dt, orc_load(dt, in[0], i));",
+         "        float acc = orc_load(dt, in[0], i);"),
     "all-gather skips a peer":
         ("if (j == r || e == b) continue;", "if (j == r || j == 0 || e == b) continue;"),
 }
@@ -66,6 +73,8 @@ def _battery(points):
         lambda: [ts.test_rsag_chunks_partition_the_range(d) for d in ts.DTYPES],
         lambda: [ts.test_reduce_scatter_then_all_gather_is_allreduce(d, 8, 4097) for d in ts.DTYPES],
         lambda: [ts.test_ll_pack_byte_image(d, 5) for d in ts.DTYPES],
+        lambda: [ta.test_stepwise_reference(d, a, 8) for d, a in ta.CASES],
+        lambda: ta.test_native_e4m3fn_rounds_every_partial_sum(),
     ]
     failed = 0
     for c in checks:
