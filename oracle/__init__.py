@@ -29,10 +29,10 @@ _SRC = os.path.join(_HERE, "sar_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-BF16, FP16, FP32, E4M3FN = 0, 1, 2, 3
-DTYPES = {"bf16": BF16, "fp16": FP16, "fp32": FP32, "e4m3fn": E4M3FN}
-ESIZE = {BF16: 2, FP16: 2, FP32: 4, E4M3FN: 1}
-NP_STORAGE = {BF16: np.uint16, FP16: np.uint16, FP32: np.float32, E4M3FN: np.uint8}
+BF16, FP16, FP32, E4M3FN, E4M3B15 = 0, 1, 2, 3, 4
+DTYPES = {"bf16": BF16, "fp16": FP16, "fp32": FP32, "e4m3fn": E4M3FN, "e4m3b15": E4M3B15}
+ESIZE = {BF16: 2, FP16: 2, FP32: 4, E4M3FN: 1, E4M3B15: 1}
+NP_STORAGE = {BF16: np.uint16, FP16: np.uint16, FP32: np.float32, E4M3FN: np.uint8, E4M3B15: np.uint8}
 
 OK, BAD_ARG, NOT_ARRIVED = 0, 1, 2
 
@@ -70,6 +70,8 @@ def _bind(lib):
     lib.orc_f32_to_bf16.argtypes, lib.orc_f32_to_bf16.restype = [ctypes.c_float], ctypes.c_uint16
     lib.orc_f32_to_fp16.argtypes, lib.orc_f32_to_fp16.restype = [ctypes.c_float], ctypes.c_uint16
     lib.orc_f32_to_e4m3fn.argtypes, lib.orc_f32_to_e4m3fn.restype = [ctypes.c_float], ctypes.c_uint8
+    lib.orc_e4m3b15_to_f32.argtypes, lib.orc_e4m3b15_to_f32.restype = [ctypes.c_uint8], ctypes.c_float
+    lib.orc_f32_to_e4m3b15.argtypes, lib.orc_f32_to_e4m3b15.restype = [ctypes.c_float], ctypes.c_uint8
     lib.orc_round_array.argtypes, lib.orc_round_array.restype = [i32, vp, vp, sz], None
     lib.orc_decode_array.argtypes, lib.orc_decode_array.restype = [i32, vp, vp, sz], None
     lib.orc_add_f32.argtypes, lib.orc_add_f32.restype = [ctypes.c_float, ctypes.c_float], ctypes.c_float

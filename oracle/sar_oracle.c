@@ -49,8 +49,15 @@
  *                S.1111.110 = 448, subnormals m/8 * 2^-6.  Conversion from
  *                binary32 saturates finite overflow and infinities to +-448
  *                ("satfinite"); NaN stays NaN.
- *    Canonical NaN outputs: bf16 0x7FC0, fp16 0x7E00, e4m3fn 0x7F, f32
- *    0x7FC00000 (sign dropped).  Tests compare NaN by class.
+ *      e4m3b15 : mscclpp commit history, "Add fp8_e4m3b15 datatype": 1 sign,
+ *                4 exponent (bias 15), 3 fraction bits, max finite 0.9375.
+ *                Max finite 0.9375 = 1.875 * 2^-1 puts the largest finite
+ *                exponent field at 14, so field 15 is not finite; read
+ *                IEEE-style: S.1111.000 = infinity, S.1111.mmm (mmm != 0) =
+ *                NaN, subnormals m/8 * 2^-14, binary32 overflow rounds to
+ *                infinity.
+ *    Canonical NaN outputs: bf16 0x7FC0, fp16 0x7E00, e4m3fn 0x7F, e4m3b15
+ *    0x7F, f32 0x7FC00000 (sign dropped).  Tests compare NaN by class.
  *
  * Parity pins (in the tests, independent of this file): brute-force nearest
  * search over each format's code table written from the field definitions,
@@ -65,7 +72,7 @@
 #include <string.h>
 
 /* Element types; the integer codes are the oracle's own. */
-enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_FP32 = 2, ORC_E4M3FN = 3 };
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_FP32 = 2, ORC_E4M3FN = 3, ORC_E4M3B15 = 4 };
 
 /* Return codes. */
 enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_NOT_ARRIVED = 2 };
@@ -79,6 +86,7 @@ int orc_esize(int dt) {
     case ORC_FP16: return 2;
     case ORC_FP32: return 4;
     case ORC_E4M3FN: return 1;
+    case ORC_E4M3B15: return 1;
     default: return 0;
     }
 }
@@ -118,6 +126,22 @@ float orc_e4m3fn_to_f32(uint8_t c) {
     if (e == 0xF && f == 0x7) return bits_f32(0x7FC00000u);
     if (e == 0) mag = ldexpf((float)f, -9);
     else mag = ldexpf((float)(8 + f), e - 10);
+    return s ? -mag : mag;
+}
+
+/* e4m3b15: E == 0 -> f * 2^-17; 0 < E < 15 -> (8 + f) * 2^(E-18);
+ * E == 15 -> infinity (f == 0) or NaN. */
+float orc_e4m3b15_to_f32(uint8_t c) {
+    int s = (c >> 7) & 1, e = (c >> 3) & 0xF, f = c & 0x7;
+    float mag;
+    if (e == 0xF) {
+        if (f != 0) return bits_f32(0x7FC00000u);
+        mag = INFINITY;
+    } else if (e == 0) {
+        mag = ldexpf((float)f, -17);
+    } else {
+        mag = ldexpf((float)(8 + f), e - 18);
+    }
     return s ? -mag : mag;
 }
 
@@ -229,6 +253,20 @@ uint8_t orc_f32_to_e4m3fn(float x) {
     return s | (uint8_t)c;
 }
 
+uint8_t orc_f32_to_e4m3b15(float x) {
+    static const orc_fmt F = { 4, -14, 15 };
+    uint32_t u = f32_bits(x);
+    uint8_t s = (uint8_t)((u >> 24) & 0x80);
+    float ax = fabsf(x);
+    if (isnan(x)) return 0x7F;
+    if (isinf(x)) return s | 0x78;
+    if (ax == 0.0f) return s;
+    int q; uint64_t n = round_to_grid(ax, &F, &q);
+    int64_t c = encode_grid(n, q, &F, 14);
+    if (c < 0) return s | 0x78;                       /* overflow -> infinity */
+    return s | (uint8_t)c;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Element access on byte arrays.                                             */
 /* ------------------------------------------------------------------------ */
@@ -240,6 +278,7 @@ float orc_load(int dt, const void* base, size_t i) {
     case ORC_FP16: { uint16_t h; memcpy(&h, b + 2 * i, 2); return orc_fp16_to_f32(h); }
     case ORC_FP32: { float x; memcpy(&x, b + 4 * i, 4); return x; }
     case ORC_E4M3FN: return orc_e4m3fn_to_f32(b[i]);
+    case ORC_E4M3B15: return orc_e4m3b15_to_f32(b[i]);
     }
     return NAN;
 }
@@ -254,6 +293,7 @@ void orc_store(int dt, void* base, size_t i, float x) {
         memcpy(b + 4 * i, &x, 4); break;
     }
     case ORC_E4M3FN: b[i] = orc_f32_to_e4m3fn(x); break;
+    case ORC_E4M3B15: b[i] = orc_f32_to_e4m3b15(x); break;
     }
 }
 

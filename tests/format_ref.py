@@ -13,6 +13,8 @@ Formats:
   semantics, overflow rounds to infinity.
   e4m3fn (OCP 8-bit floating point, E4M3): 1/4/3, bias 7, no infinities,
   S.1111.111 is NaN, max finite 448; conversion saturates to +-448.
+  e4m3b15: 1/4/3, bias 15, max finite 0.9375 (the page's definition), so the
+  all-ones exponent is infinity / NaN and overflow rounds to infinity.
 """
 from __future__ import annotations
 
@@ -25,6 +27,8 @@ FORMATS = {
     "bf16": (8, 7, 127, True),
     "fp16": (5, 10, 15, True),
     "e4m3fn": (4, 3, 7, False),
+    # bias 15, max finite 0.9375: the all-ones exponent is infinity / NaN
+    "e4m3b15": (4, 3, 15, True),
 }
 
 

@@ -29,7 +29,7 @@ def _f32_points() -> np.ndarray:
     up = np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)
     for low in (0x0000, 0x0001, 0x0FFF, 0x1000, 0x1001, 0x7FFF, 0x8000, 0x8001, 0xFFFF):
         pts.append(up | np.uint32(low))
-    for fmt in ("bf16", "fp16", "e4m3fn"):
+    for fmt in ("bf16", "fp16", "e4m3fn", "e4m3b15"):
         vals, _ = ref.positive_table(fmt)
         mids = (vals[:-1] + vals[1:]) / 2
         over = vals[-1] + (vals[-1] - vals[-2]) / 2
@@ -58,7 +58,7 @@ def points():
     return _f32_points()
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp16", "e4m3fn"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp16", "e4m3fn", "e4m3b15"])
 def test_round_matches_bruteforce_nearest(points, fmt):
     got = oracle.round_f32(points, fmt).astype(np.int64)
     want = ref.nearest_even(points.astype(np.float64), fmt)
@@ -88,7 +88,7 @@ def test_round_e4m3fn_matches_torch_in_range(points):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp16", "e4m3fn"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp16", "e4m3fn", "e4m3b15"])
 def test_decode_every_code(fmt):
     n = ref.n_codes(fmt)
     codes = np.arange(n).astype(oracle.NP_STORAGE[oracle.DTYPES[fmt]])
@@ -119,7 +119,7 @@ def test_decode_matches_libraries():
     assert np.array_equal(np.isnan(o8), ~ok) and np.array_equal(o8[ok], lib8[ok])
 
 
-@pytest.mark.parametrize("fmt,canon", [("bf16", 0x7FC0), ("fp16", 0x7E00), ("e4m3fn", 0x7F)])
+@pytest.mark.parametrize("fmt,canon", [("bf16", 0x7FC0), ("fp16", 0x7E00), ("e4m3fn", 0x7F), ("e4m3b15", 0x7F)])
 def test_round_trip_every_code(fmt, canon):
     """decode then encode is the identity on every code except NaN, which
     becomes the canonical NaN."""
@@ -138,6 +138,10 @@ def test_nan_and_infinity_rules():
     assert list(oracle.round_f32(specials, "fp16")) == [0x7E00, 0x7E00, 0x7C00, 0xFC00]
     # e4m3fn has no infinity: satfinite sends +-inf to +-448.
     assert list(oracle.round_f32(specials, "e4m3fn")) == [0x7F, 0x7F, 0x7E, 0xFE]
+    # e4m3b15 keeps infinities (S.1111.000); overflow past 0.96875 rounds to them
+    assert list(oracle.round_f32(specials, "e4m3b15")) == [0x7F, 0x7F, 0x78, 0xF8]
+    big = np.array([0.96875, 0.968, 1.0, -5.0], dtype=np.float32)
+    assert list(oracle.round_f32(big, "e4m3b15")) == [0x78, 0x77, 0x78, 0xF8]
 
 
 def test_subnormals_survive():
@@ -149,6 +153,21 @@ def test_subnormals_survive():
     assert list(oracle.round_f32(xs, "fp16")) == [1, 0, 1]
     xs = np.array([2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11], dtype=np.float32)
     assert list(oracle.round_f32(xs, "e4m3fn")) == [1, 0, 1]
+    xs = np.array([2.0 ** -17, 2.0 ** -18, 3 * 2.0 ** -19], dtype=np.float32)
+    assert list(oracle.round_f32(xs, "e4m3b15")) == [1, 0, 1]
+
+
+def test_e4m3b15_is_the_top_of_a_binary16():
+    """The page converts e4m3b15 through fp16: with the same bias (15), every
+    finite code is the binary16 whose bits are the code's sign, exponent and
+    fraction shifted into place (checked against numpy's binary16)."""
+    c = np.arange(256, dtype=np.uint16)
+    finite = ((c >> 3) & 0xF) != 0xF
+    half_bits = ((c & 0x80) << 8) | ((c & 0x7F) << 7)
+    lib = half_bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    got = oracle.decode(c.astype(np.uint8), "e4m3b15")
+    assert np.array_equal(got[finite], lib[finite])
+    assert finite.sum() == 240 and float(np.max(got[finite])) == 0.9375
 
 
 def _golden():

@@ -54,6 +54,10 @@ MUTANTS = {
     "accumulator seed not rounded":
         ("        float acc = round_through(acc_dt, orc_load(dt, in[0], i));",
          "        float acc = orc_load(dt, in[0], i);"),
+    "e4m3b15 largest exponent field treated as finite":
+        ("    int64_t c = encode_grid(n, q, &F, 14);", "    int64_t c = encode_grid(n, q, &F, 15);"),
+    "e4m3b15 subnormal scale":
+        ("        mag = ldexpf((float)f, -17);", "        mag = ldexpf((float)f, -16);"),
     "all-gather skips a peer":
         ("if (j == r || e == b) continue;", "if (j == r || j == 0 || e == b) continue;"),
 }
@@ -62,8 +66,9 @@ MUTANTS = {
 def _battery(points):
     """Run a selection of pins; return how many failed."""
     checks = [
-        lambda: [tf.test_round_matches_bruteforce_nearest(points, f) for f in ("bf16", "fp16", "e4m3fn")],
-        lambda: [tf.test_decode_every_code(f) for f in ("bf16", "fp16", "e4m3fn")],
+        lambda: [tf.test_round_matches_bruteforce_nearest(points, f) for f in ("bf16", "fp16", "e4m3fn", "e4m3b15")],
+        lambda: [tf.test_decode_every_code(f) for f in ("bf16", "fp16", "e4m3fn", "e4m3b15")],
+        lambda: tf.test_e4m3b15_is_the_top_of_a_binary16(),
         lambda: tf.test_golden_format_constants(),
         lambda: [ts.test_one_rank_is_identity(d) for d in ts.DTYPES],
         lambda: [ts.test_all_equal_inputs_give_n_times_x(d, 8) for d in ts.DTYPES],

@@ -17,7 +17,7 @@ import oracle
 from tests import format_ref as ref
 
 DTYPES = ["bf16", "fp16", "fp32", "e4m3fn"]
-STORE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8}
+STORE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8, "e4m3b15": np.uint8}
 
 
 def _codes_from_values(vals: np.ndarray, dt: str) -> np.ndarray:
@@ -66,7 +66,7 @@ def test_one_rank_is_identity(dt):
     assert _same_bits(x, y)
 
 
-@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("dt", DTYPES + ["e4m3b15"])
 @pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 32])
 def test_all_equal_inputs_give_n_times_x(dt, n):
     rng = np.random.default_rng(n)
@@ -100,6 +100,32 @@ def test_small_integers_sum_exactly_under_any_rank_order(dt, n):
     perm = rng.permutation(n)
     outs_p = oracle.allreduce([ins[p] for p in perm], dt)
     assert _same_bits(outs_p[0], outs[0])
+
+
+@pytest.mark.parametrize("n", [2, 5, 8, 32])
+def test_e4m3b15_small_multiples_sum_exactly(n):
+    """Multiples of 2^-9 up to 15 * 2^-9 are e4m3b15 values; their sums are
+    exact in binary32, so the result is R_e4m3b15(exact sum), under any rank
+    order."""
+    rng = np.random.default_rng(40 + n)
+    vals = rng.integers(-15, 16, size=(n, 3000)).astype(np.float64) * 2.0 ** -9
+    ins = [_codes_from_values(v, "e4m3b15") for v in vals]
+    want = _expected(vals.sum(axis=0), "e4m3b15")
+    outs = oracle.allreduce(ins, "e4m3b15")
+    assert _same_bits(outs[0], want) and _same_bits(outs[-1], want)
+    perm = rng.permutation(n)
+    assert _same_bits(oracle.allreduce([ins[p] for p in perm], "e4m3b15")[0], want)
+
+
+def test_all_e4m3b15_pairs_bruteforce():
+    vals = ref.all_values("e4m3b15")
+    good = np.nonzero(np.isfinite(vals))[0]
+    a, b = np.meshgrid(good, good, indexing="ij")
+    a, b = a.ravel().astype(np.uint8), b.ravel().astype(np.uint8)
+    exact = vals[a.astype(np.int64)] + vals[b.astype(np.int64)]
+    want = ref.nearest_even(exact, "e4m3b15").astype(np.uint8)
+    y0, _ = oracle.allreduce([a, b], "e4m3b15")
+    assert np.array_equal(y0, want)
 
 
 def test_all_e4m3fn_pairs_bruteforce():
