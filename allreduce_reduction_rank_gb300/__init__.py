@@ -11,6 +11,7 @@ Function names follow the C ABI: :func:`sar_allreduce`,
 :func:`sar_reduce_scatter`, :func:`sar_all_gather`, :func:`sar_rsag_chunk`,
 :func:`sar_ll_packet_bytes`, :func:`sar_ll_pack`,
 :func:`sar_ll_unpack_reduce`, :func:`sar_allreduce_ll`,
+:func:`sar_allreduce_ll_noalloc`,
 :func:`sar_fp8_convert`, :func:`sar_read_device_status`,
 :func:`sar_status_string`.
 """
@@ -39,6 +40,7 @@ SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE = 0, 1
 (SAR_OK, SAR_ERR_INVALID_ARG, SAR_ERR_UNSUPPORTED_NRANKS, SAR_ERR_UNSUPPORTED_DTYPE,
  SAR_ERR_MISALIGNED, SAR_ERR_CUDA, SAR_ERR_TIMEOUT) = range(7)
 SAR_MAX_RANKS = 32
+SAR_LL_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 DTYPE_CODES = {"bf16": SAR_BF16, "fp16": SAR_FP16, "fp32": SAR_FP32, "e4m3fn": SAR_FP8_E4M3FN}
 TORCH_DTYPES = {SAR_BF16: torch.bfloat16, SAR_FP16: torch.float16, SAR_FP32: torch.float32,
@@ -58,12 +60,13 @@ lib.sar_ll_packet_bytes.restype = _sz
 lib.sar_ll_pack.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _vp]
 lib.sar_ll_unpack_reduce.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
 lib.sar_allreduce_ll.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
+lib.sar_allreduce_ll_noalloc.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u64, _vp, _vp]
 lib.sar_fp8_convert.argtypes = [_vp, _i32, _vp, _i32, _sz, _vp]
 lib.sar_read_device_status.argtypes = [_vp, _vp]
 lib.sar_status_string.argtypes = [_i32]
 lib.sar_status_string.restype = ctypes.c_char_p
 for _f in ("sar_allreduce", "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
-           "sar_allreduce_ll", "sar_fp8_convert", "sar_read_device_status"):
+           "sar_allreduce_ll", "sar_allreduce_ll_noalloc", "sar_fp8_convert", "sar_read_device_status"):
     getattr(lib, _f).restype = _i32
 
 
@@ -175,6 +178,17 @@ def sar_allreduce_ll(ins, outs, pkts, epoch: int, status, max_spins: int = 1 << 
     ppk, _ = _ptrs(pkts)
     _check(lib.sar_allreduce_ll(pin, pout, ppk, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), epoch,
                                 max_spins, _addr(status), _stream(stream)))
+
+
+def sar_allreduce_ll_noalloc(ins, outs, status=None, max_spins: int = 1 << 20, count=None, dtype=None,
+                             stream=None) -> None:
+    """LL allreduce with the library's fixed packet scratch, for callers that
+    cannot allocate device memory (see include/sar.h).  ``status`` is an
+    optional device int32 that receives SAR_ERR_TIMEOUT."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    _check(lib.sar_allreduce_ll_noalloc(pin, pout, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), max_spins,
+                                        None if status is None else _addr(status), _stream(stream)))
 
 
 def sar_fp8_convert(src, dst, src_dtype=None, dst_dtype=None, count=None, stream=None) -> None:

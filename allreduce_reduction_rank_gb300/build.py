@@ -27,7 +27,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsar.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["sar_api.cu", "rsag.cu", "ll.cu", "convert.cu"]
+SOURCES = ["sar_api.cu", "rsag.cu", "ll.cu", "convert.cu", "noalloc.cu"]
 HEADERS = ["sar_device.cuh", "sar_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

@@ -191,6 +191,46 @@ SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, voi
                             int32_t* d_status, sar_stream_t stream);
 
 /*
+ * Size of the fixed LL packet scratch inside the library used by
+ * sar_allreduce_ll_noalloc: 16 MiB per GPU.  A call fits when
+ * nranks * (sar_ll_packet_bytes(count, dtype) rounded up to 256) is at most
+ * this size, e.g. up to 1 MiB per rank with 8 ranks.
+ */
+#define SAR_LL_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * sar_allreduce_ll_noalloc -- sar_allreduce_ll without caller-provided packet
+ * scratch, for callers that cannot allocate device memory: code inside a
+ * framework whose allocator owns the device memory, plugins with a fixed
+ * memory budget, or paths where a cudaMalloc would synchronise the device or
+ * is not allowed.  The paper has no counterpart of this entry point.
+ *
+ * The outputs equal sar_allreduce_ll's bit for bit.  The call allocates
+ * nothing: the packet scratch is a fixed array of SAR_LL_NOALLOC_SCRATCH_BYTES
+ * (plus one status word) compiled into the library, which every GPU that
+ * loads the library's device code holds until the process exits.  The caller
+ * still passes the inputs and outputs.
+ *
+ * - Sizes beyond the array (see SAR_LL_NOALLOC_SCRATCH_BYTES) return
+ *   SAR_ERR_INVALID_ARG before anything is launched.
+ * - The first call on a device looks up the array's device address on that
+ *   device (the current one); make that first call before any CUDA graph
+ *   capture on the device.
+ * - The epoch is managed by the library (a new one per call and device).
+ * - d_status: an optional caller device int32 that receives SAR_ERR_TIMEOUT if
+ *   a poll runs out of spins (as in sar_ll_unpack_reduce).  With NULL, an
+ *   internal status word is cleared and used instead, and a timeout is not
+ *   reported to the caller.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   packets.  Calls that overlap on the GPU (for example on two streams
+ *   without ordering between them) race on it: their outputs are undefined
+ *   and their polls may time out.
+ */
+SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, void* const* out, int nranks,
+                                            size_t count, sar_dtype dtype, uint64_t max_spins,
+                                            int32_t* d_status, sar_stream_t stream);
+
+/*
  * sar_fp8_convert -- dst[i] = R_dst(f32(src[i])) for count elements.
  *
  * Supported pairs: e4m3fn -> {fp32, fp16, bf16} (exact) and
