@@ -8,7 +8,8 @@ Importing this package fails if ``_build/libsar.so`` has not been built
 (``python allreduce_reduction_rank_gb300/build.py``).
 
 Function names follow the C ABI: :func:`sar_allreduce`,
-:func:`sar_reduce_scatter`, :func:`sar_all_gather`, :func:`sar_rsag_chunk`,
+:func:`sar_allreduce_accum`, :func:`sar_reduce_scatter`, :func:`sar_all_gather`,
+:func:`sar_rsag_chunk`, :func:`sar_allreduce_ll_fused`, :func:`sar_allreduce_ll_writeback`,
 :func:`sar_ll_packet_bytes`, :func:`sar_ll_pack`,
 :func:`sar_ll_unpack_reduce`, :func:`sar_allreduce_ll`,
 :func:`sar_allreduce_ll_noalloc`,
@@ -33,7 +34,7 @@ if not os.path.exists(LIB_PATH):
 lib = ctypes.CDLL(LIB_PATH)
 
 # sar_dtype
-SAR_BF16, SAR_FP16, SAR_FP32, SAR_FP8_E4M3FN = 0, 1, 2, 3
+SAR_BF16, SAR_FP16, SAR_FP32, SAR_FP8_E4M3FN, SAR_FP8_E4M3B15 = 0, 1, 2, 3, 4
 # sar_algo
 SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE = 0, 1
 # sar_status
@@ -42,15 +43,17 @@ SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE = 0, 1
 SAR_MAX_RANKS = 32
 SAR_LL_NOALLOC_SCRATCH_BYTES = 16 << 20
 
-DTYPE_CODES = {"bf16": SAR_BF16, "fp16": SAR_FP16, "fp32": SAR_FP32, "e4m3fn": SAR_FP8_E4M3FN}
+DTYPE_CODES = {"bf16": SAR_BF16, "fp16": SAR_FP16, "fp32": SAR_FP32, "e4m3fn": SAR_FP8_E4M3FN,
+               "e4m3b15": SAR_FP8_E4M3B15}
 TORCH_DTYPES = {SAR_BF16: torch.bfloat16, SAR_FP16: torch.float16, SAR_FP32: torch.float32,
                 SAR_FP8_E4M3FN: torch.float8_e4m3fn}
-ESIZE = {SAR_BF16: 2, SAR_FP16: 2, SAR_FP32: 4, SAR_FP8_E4M3FN: 1}
+ESIZE = {SAR_BF16: 2, SAR_FP16: 2, SAR_FP32: 4, SAR_FP8_E4M3FN: 1, SAR_FP8_E4M3B15: 1}
 
 _vp, _sz, _i32, _u32, _u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64
 _vpp = ctypes.POINTER(ctypes.c_void_p)
 
 lib.sar_allreduce.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _i32, _vp]
+lib.sar_allreduce_accum.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _i32, _vp]
 lib.sar_reduce_scatter.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _vp]
 lib.sar_all_gather.argtypes = [_vpp, _i32, _sz, _i32, _vp]
 lib.sar_rsag_chunk.argtypes = [_sz, _i32, _i32]
@@ -60,12 +63,14 @@ lib.sar_ll_packet_bytes.restype = _sz
 lib.sar_ll_pack.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _vp]
 lib.sar_ll_unpack_reduce.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
 lib.sar_allreduce_ll.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
+lib.sar_allreduce_ll_fused.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _vp, _u64, _vp, _vp]
+lib.sar_allreduce_ll_writeback.argtypes = [_vpp, _vpp, _vpp, _vp, _i32, _sz, _i32, _u32, _vp, _i32, _u64, _vp, _vp]
 lib.sar_allreduce_ll_noalloc.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u64, _vp, _vp]
 lib.sar_fp8_convert.argtypes = [_vp, _i32, _vp, _i32, _sz, _vp]
 lib.sar_read_device_status.argtypes = [_vp, _vp]
 lib.sar_status_string.argtypes = [_i32]
 lib.sar_status_string.restype = ctypes.c_char_p
-for _f in ("sar_allreduce", "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
+for _f in ("sar_allreduce", "sar_allreduce_accum", "sar_allreduce_ll_fused", "sar_allreduce_ll_writeback", "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
            "sar_allreduce_ll", "sar_allreduce_ll_noalloc", "sar_fp8_convert", "sar_read_device_status"):
     getattr(lib, _f).restype = _i32
 
@@ -144,6 +149,14 @@ def sar_allreduce(ins, outs, count=None, dtype=None, algo=SAR_ALGO_RSAG, stream=
                              _stream(stream)))
 
 
+def sar_allreduce_accum(ins, outs, accum, count=None, dtype=None, stream=None) -> None:
+    """Fused rsag allreduce with every partial sum rounded into `accum`."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    _check(lib.sar_allreduce_accum(pin, pout, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]),
+                                   _dtype_code(accum), _stream(stream)))
+
+
 def sar_reduce_scatter(ins, outs, count=None, dtype=None, stream=None) -> None:
     pin, n = _ptrs(ins)
     pout, _ = _ptrs(outs)
@@ -178,6 +191,30 @@ def sar_allreduce_ll(ins, outs, pkts, epoch: int, status, max_spins: int = 1 << 
     ppk, _ = _ptrs(pkts)
     _check(lib.sar_allreduce_ll(pin, pout, ppk, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), epoch,
                                 max_spins, _addr(status), _stream(stream)))
+
+
+def sar_allreduce_ll_fused(ins, outs, pkts, status, epoch: int = 0, epoch_ctrl=None, max_spins: int = 1 << 20,
+                           count=None, dtype=None, stream=None) -> None:
+    """LL allreduce in one cooperative launch.  `epoch_ctrl`: optional device
+    uint32[2] control block; when given the epoch advances on the device."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    ppk, _ = _ptrs(pkts)
+    _check(lib.sar_allreduce_ll_fused(pin, pout, ppk, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), epoch,
+                                      None if epoch_ctrl is None else _addr(epoch_ctrl), max_spins, _addr(status),
+                                      _stream(stream)))
+
+
+def sar_allreduce_ll_writeback(ins, outs, pkts, res, status, multi_dest: bool = True, epoch: int = 0,
+                               epoch_ctrl=None, max_spins: int = 1 << 20, count=None, dtype=None, stream=None) -> None:
+    """LL allreduce whose write-back is a second packet round through `res`."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    ppk, _ = _ptrs(pkts)
+    _check(lib.sar_allreduce_ll_writeback(pin, pout, ppk, _addr(res), n, _count(count, ins[0]),
+                                          _dtype_code(dtype, ins[0]), epoch,
+                                          None if epoch_ctrl is None else _addr(epoch_ctrl), int(bool(multi_dest)),
+                                          max_spins, _addr(status), _stream(stream)))
 
 
 def sar_allreduce_ll_noalloc(ins, outs, status=None, max_spins: int = 1 << 20, count=None, dtype=None,

@@ -27,8 +27,11 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsar.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["sar_api.cu", "rsag.cu", "ll.cu", "convert.cu", "noalloc.cu"]
-HEADERS = ["sar_device.cuh", "sar_internal.h"]
+# Slowest first, so the parallel build finishes sooner.
+SOURCES = ["rsag_e4m3b15.cu", "rsag_e4m3b15_acc.cu", "ll_writeback.cu", "ll_fused.cu", "ll.cu", "rsag_e4m3fn_acc.cu",
+           "rsag_e4m3fn.cu", "rsag_bf16_acc.cu", "rsag_fp16_acc.cu", "rsag_fp32_acc.cu", "rsag_fp16.cu",
+           "rsag_bf16.cu", "rsag_fp32.cu", "convert.cu", "rsag.cu", "sar_api.cu", "noalloc.cu"]
+HEADERS = ["sar_device.cuh", "sar_internal.h", "rsag_kernels.cuh", "ll_coop.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-std=c++17", "-lineinfo",
@@ -75,7 +78,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             os.replace(obj + ".tmp", obj)
         return obj
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
+    with ThreadPoolExecutor(min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     if force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"

@@ -121,11 +121,12 @@ ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
 // ---------------------------------------------------------------------------
 template <int DT, int NR>
 __global__ void __launch_bounds__(kThreads)
-ll_unpack_reduce_kernel(const RankPtrs p, size_t count, size_t nbytes, size_t chunk_q, uint32_t epoch,
+ll_unpack_reduce_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t epoch,
                         uint64_t max_spins, int32_t* status, bool vec_out) {
     constexpr int VE = Elem<DT>::kVE;
     constexpr int EP = PerWord<DT>::kN;
-    constexpr int WIN = NR < 8 ? NR : 8;
+    constexpr int WIN = NR == 0 ? 4 : (NR < 8 ? NR : 8);
+    const int n = ranks<NR>(n_rt);
     const int r = blockIdx.y;
     const size_t npk = (nbytes + 3) / 4;
     const size_t nq = (npk + 3) / 4;
@@ -138,17 +139,20 @@ ll_unpack_reduce_kernel(const RankPtrs p, size_t count, size_t nbytes, size_t ch
         if (16 * (q + 1) <= nbytes) {
             // A whole group: 4 packets of payload from every rank.
             Acc<DT> acc;
-#pragma unroll
-            for (int k0 = 0; k0 < NR; k0 += WIN) {
+// Windows of 8 ranks run as a loop (one window for up to 8 ranks).
+#pragma unroll 1
+            for (int k0 = 0; k0 < n; k0 += WIN) {
                 uint64_t w[WIN][4];
 #pragma unroll
                 for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
                     const uint64_t* src = static_cast<const uint64_t*>(p.in[k0 + k]) + 4 * q;
                     ld_packets2(src, w[k][0], w[k][1]);
                     ld_packets2(src + 2, w[k][2], w[k][3]);
                 }
 #pragma unroll
                 for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
                     const uint64_t* src = static_cast<const uint64_t*>(p.in[k0 + k]) + 4 * q;
                     if (!poll_quad(src, epoch, max_spins, status, w[k])) return;
                     const uint4 x = make_uint4(packet_payload(w[k][0]), packet_payload(w[k][1]),
@@ -160,19 +164,19 @@ ll_unpack_reduce_kernel(const RankPtrs p, size_t count, size_t nbytes, size_t ch
             if (vec_out) {
                 const uint4 y = acc_round<DT>(acc);
 #pragma unroll
-                for (int j = 0; j < NR; ++j) st_stream(static_cast<uint4*>(p.out[j]) + q, y);
+                for (int j = 0; j < n; ++j) st_stream(static_cast<uint4*>(p.out[j]) + q, y);
             } else {
 #pragma unroll
                 for (int e = 0; e < VE; ++e)
 #pragma unroll
-                    for (int j = 0; j < NR; ++j) store_elem<DT>(p.out[j], q * VE + e, acc.v[e]);
+                    for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], q * VE + e, acc.v[e]);
             }
         } else {
             // The last group: 1..4 packets, the last one possibly padded.
             const size_t wend = min(npk, 4 * q + 4);
             for (size_t w = 4 * q; w < wend; ++w) {
                 float acc[EP];
-                for (int k = 0; k < NR; ++k) {
+                for (int k = 0; k < n; ++k) {
                     const uint64_t* src = static_cast<const uint64_t*>(p.in[k]) + w;
                     uint64_t pk = ld_packet(src);
                     if (!poll_one(src, epoch, max_spins, status, pk)) return;
@@ -185,7 +189,7 @@ ll_unpack_reduce_kernel(const RankPtrs p, size_t count, size_t nbytes, size_t ch
                 for (int e = 0; e < EP; ++e) {
                     const size_t i = w * EP + e;
                     if (i < count)
-                        for (int j = 0; j < NR; ++j) store_elem<DT>(p.out[j], i, acc[e]);
+                        for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], i, acc[e]);
                 }
             }
         }
@@ -202,14 +206,14 @@ inline unsigned grid_x(size_t items, size_t cap) {
 constexpr size_t kGridCap = 65535;
 
 template <int DT, int NR>
-cudaError_t unpack_dispatch(const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
+cudaError_t unpack_dispatch(int nranks, const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
                             int32_t* status, bool vec_out, cudaStream_t s) {
     const size_t nbytes = count * Elem<DT>::kSize;
     const size_t npk = (nbytes + 3) / 4, nq = (npk + 3) / 4;
-    const size_t chunk_q = (nq + NR - 1) / NR;
-    const dim3 grid(grid_x(chunk_q, kGridCap), NR);
+    const size_t chunk_q = (nq + nranks - 1) / nranks;
+    const dim3 grid(grid_x(chunk_q, kGridCap), nranks);
     ll_unpack_reduce_kernel<DT, NR>
-        <<<grid, kThreads, 0, s>>>(p, count, nbytes, chunk_q, epoch, max_spins, status, vec_out);
+        <<<grid, kThreads, 0, s>>>(p, nranks, count, nbytes, chunk_q, epoch, max_spins, status, vec_out);
     return cudaGetLastError();
 }
 
@@ -217,13 +221,15 @@ template <int DT>
 cudaError_t unpack_ranks(int nranks, const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
                          int32_t* status, bool vec_out, cudaStream_t s) {
     switch (nranks) {
-    case 1: return unpack_dispatch<DT, 1>(p, count, epoch, max_spins, status, vec_out, s);
-    case 2: return unpack_dispatch<DT, 2>(p, count, epoch, max_spins, status, vec_out, s);
-    case 4: return unpack_dispatch<DT, 4>(p, count, epoch, max_spins, status, vec_out, s);
-    case 8: return unpack_dispatch<DT, 8>(p, count, epoch, max_spins, status, vec_out, s);
-    case 16: return unpack_dispatch<DT, 16>(p, count, epoch, max_spins, status, vec_out, s);
-    case 32: return unpack_dispatch<DT, 32>(p, count, epoch, max_spins, status, vec_out, s);
-    default: return cudaErrorInvalidValue;
+    case 1: return unpack_dispatch<DT, 1>(1, p, count, epoch, max_spins, status, vec_out, s);
+    case 2: return unpack_dispatch<DT, 2>(2, p, count, epoch, max_spins, status, vec_out, s);
+    case 4: return unpack_dispatch<DT, 4>(4, p, count, epoch, max_spins, status, vec_out, s);
+    case 8: return unpack_dispatch<DT, 8>(8, p, count, epoch, max_spins, status, vec_out, s);
+    case 16: return unpack_dispatch<DT, 16>(16, p, count, epoch, max_spins, status, vec_out, s);
+    case 32: return unpack_dispatch<DT, 32>(32, p, count, epoch, max_spins, status, vec_out, s);
+    default:
+        if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
+        return unpack_dispatch<DT, 0>(nranks, p, count, epoch, max_spins, status, vec_out, s);
     }
 }
 
@@ -250,6 +256,8 @@ cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p,
     case SAR_FP32: return unpack_ranks<SAR_FP32>(nranks, p, count, epoch, max_spins, status, vec_out, stream);
     case SAR_FP8_E4M3FN:
         return unpack_ranks<SAR_FP8_E4M3FN>(nranks, p, count, epoch, max_spins, status, vec_out, stream);
+    case SAR_FP8_E4M3B15:
+        return unpack_ranks<SAR_FP8_E4M3B15>(nranks, p, count, epoch, max_spins, status, vec_out, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -1,0 +1,377 @@
+// ll_coop.cuh -- the LL all-pair allreduce as one cooperative launch: the
+// kernel template shared by sar_allreduce_ll_fused (ll_fused.cu) and
+// sar_allreduce_ll_writeback (ll_writeback.cu).
+//
+// mscclpp commit history, the allreduce_allpair_packet fix: the same thread
+// block sends, reduces and writes back.  Every block of simulated rank r
+//   A. packs its share of rank r's input into pkts[r] (the send);
+//   B. polls its share of rank r's packet chunk in all N packet buffers (the
+//      packets are written by other blocks of the same launch), reduces in
+//      rank order and rounds once;
+//   C. writes the result back, in one of three ways (template WB):
+//        kDirect     - plain stores from registers to all N outputs;
+//        kPacketsAll - as flagged result packets into `res`; then a block of
+//                      rank r polls the result packets of chunk (r + 1) mod N
+//                      and writes each one, read once, to all N outputs (the
+//                      read-once, write-to-several-destinations fusion of the
+//                      commit history's ReadPutPacket change);
+//        kPacketsOwn - as result packets; then every rank j polls all result
+//                      packets and writes its own output only.
+// Each 8-byte packet is one single-copy-atomic store and load, so a flag that
+// matches the epoch guarantees its payload; a stale flag means "not arrived".
+// Every poll is bounded.  Blocks wait on one another, so the launch is
+// cooperative: the runtime makes every block co-resident or refuses the launch.
+//
+// Epochs: the caller's, or a device control block {last epoch, arrivals}
+// (commit history, the flag buffer change: one flag buffer shared by the
+// algorithms) that the kernel advances: every launch uses last + 1 and the last
+// block to finish stores it, so a replayed CUDA graph gets a fresh epoch.
+#pragma once
+
+#include <algorithm>
+#include <atomic>
+
+#include "sar_device.cuh"
+#include "sar_internal.h"
+
+namespace sar {
+namespace llc {
+
+enum WriteBack { kDirect = 0, kPacketsAll = 1, kPacketsOwn = 2 };
+
+constexpr unsigned kMaxSleepNs = 1024;
+
+__device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
+    int32_t v;
+    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_u32_v(const uint32_t* s) {
+    uint32_t v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
+    return v;
+}
+
+// Wait until packets w[0..n) (already loaded) carry `epoch`; false when this
+// thread gave up or saw another thread give up.
+template <int N>
+__device__ __forceinline__ bool poll(const uint64_t* src, uint32_t epoch, uint64_t max_spins, int32_t* status,
+                                     uint64_t (&w)[N]) {
+    unsigned ns = 32;
+    for (uint64_t spin = 0;; ++spin) {
+        bool ready = true;
+#pragma unroll
+        for (int i = 0; i < N; ++i) ready = ready && packet_flag(w[i]) == epoch;
+        if (ready) return true;
+        if (spin >= max_spins) {
+            atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+            return false;
+        }
+        if (ld_status_v(status) != 0) return false;
+        __nanosleep(ns);
+        if (ns < kMaxSleepNs) ns *= 2;
+        if constexpr (N == 4) {
+            ld_packets2(src, w[0], w[1]);
+            ld_packets2(src + 2, w[2], w[3]);
+        } else {
+            w[0] = ld_packet(src);
+        }
+    }
+}
+
+struct LLArgs {
+    RankPtrs data;                   // in[r]: inputs, out[j]: outputs
+    uint64_t* pkts[SAR_MAX_RANKS];   // send packet buffers
+    uint64_t* res;                   // result packet buffer (packet write-back only)
+};
+
+// Raw element e of a payload word, stored as bits (no conversion).
+template <int DT> __device__ __forceinline__ void store_bits(void* base, size_t i, uint32_t word, int e) {
+    constexpr int ES = Elem<DT>::kSize;
+    if constexpr (ES == 4) static_cast<uint32_t*>(base)[i] = word;
+    else if constexpr (ES == 2) static_cast<uint16_t*>(base)[i] = static_cast<uint16_t>(word >> (16 * e));
+    else static_cast<unsigned char*>(base)[i] = static_cast<unsigned char>(word >> (8 * e));
+}
+
+// Phase A: rank r's input -> pkts[r].
+__device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t epoch, bool in16, size_t tid,
+                                     size_t stride) {
+    const int r = blockIdx.y;
+    const size_t npk = (nbytes + 3) / 4;
+    uint64_t* mine = a.pkts[r];
+    const size_t nfull = nbytes / 16;
+    if (in16) {
+        const uint4* src = static_cast<const uint4*>(a.data.in[r]);
+        for (size_t q = tid; q < nfull; q += stride) {
+            const uint4 x = ld_stream(src + q);
+            st_packets2(mine + 4 * q, make_packet(x.x, epoch), make_packet(x.y, epoch));
+            st_packets2(mine + 4 * q + 2, make_packet(x.z, epoch), make_packet(x.w, epoch));
+        }
+    }
+    const unsigned char* b = static_cast<const unsigned char*>(a.data.in[r]);
+    for (size_t w = (in16 ? 4 * nfull : 0) + tid; w < npk; w += stride) {
+        uint32_t payload = 0;
+        for (int k = 0; k < 4; ++k)
+            if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
+        st_packet(mine + w, make_packet(payload, epoch));
+    }
+}
+
+// Phase B (+ C for kDirect): reduce rank r's chunk.  False when a poll gave up.
+template <int DT, int NR, int WB>
+__device__ __forceinline__ bool reduce(const LLArgs& a, int n_rt, size_t count, size_t nbytes, size_t chunk_q,
+                                       uint32_t epoch, uint64_t max_spins, int32_t* status, bool out16, size_t tid,
+                                       size_t stride) {
+    constexpr int VE = Elem<DT>::kVE;
+    constexpr int EP = PerWord<DT>::kN;
+    constexpr int WIN = NR == 0 ? 4 : (NR < 8 ? NR : 8);
+    const int n = ranks<NR>(n_rt);
+    const int r = blockIdx.y;
+    const size_t npk = (nbytes + 3) / 4;
+    const size_t nq = (npk + 3) / 4;
+    const size_t qb = static_cast<size_t>(r) * chunk_q;
+    const size_t qe = min(nq, qb + chunk_q);
+    for (size_t q = qb + tid; q < qe; q += stride) {
+        if (16 * (q + 1) <= nbytes) {
+            Acc<DT> acc;
+#pragma unroll 1
+            for (int k0 = 0; k0 < n; k0 += WIN) {
+                uint64_t w[WIN][4];
+#pragma unroll
+                for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
+                    const uint64_t* src = a.pkts[k0 + k] + 4 * q;
+                    ld_packets2(src, w[k][0], w[k][1]);
+                    ld_packets2(src + 2, w[k][2], w[k][3]);
+                }
+#pragma unroll
+                for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
+                    if (!poll<4>(a.pkts[k0 + k] + 4 * q, epoch, max_spins, status, w[k])) return false;
+                    const uint4 x = make_uint4(packet_payload(w[k][0]), packet_payload(w[k][1]),
+                                               packet_payload(w[k][2]), packet_payload(w[k][3]));
+                    if (k0 + k == 0) acc_seed<DT>(acc, x);
+                    else acc_add<DT>(acc, x);
+                }
+            }
+            const uint4 y = acc_round<DT>(acc);
+            if constexpr (WB != kDirect) {
+                st_packets2(a.res + 4 * q, make_packet(y.x, epoch), make_packet(y.y, epoch));
+                st_packets2(a.res + 4 * q + 2, make_packet(y.z, epoch), make_packet(y.w, epoch));
+            } else if (out16) {
+#pragma unroll
+                for (int j = 0; j < n; ++j) st_stream(static_cast<uint4*>(a.data.out[j]) + q, y);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VE; ++e)
+#pragma unroll
+                    for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], q * VE + e, acc.v[e]);
+            }
+        } else {
+            // The last group: 1..4 packets, the last one possibly padded.
+            const size_t wend = min(npk, 4 * q + 4);
+            for (size_t w = 4 * q; w < wend; ++w) {
+                float acc[EP];
+                for (int k = 0; k < n; ++k) {
+                    uint64_t pk[1] = {ld_packet(a.pkts[k] + w)};
+                    if (!poll<1>(a.pkts[k] + w, epoch, max_spins, status, pk)) return false;
+                    float x[EP];
+                    widen_word<DT>(packet_payload(pk[0]), x);
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) acc[e] = (k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
+                }
+                if constexpr (WB != kDirect) {
+                    // Elements past the end are zero bits, as in the send's padding.
+                    float xs[EP];
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) xs[e] = (w * EP + e < count) ? acc[e] : 0.0f;
+                    st_packet(a.res + w, make_packet(narrow_word<DT>(xs), epoch));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        const size_t i = w * EP + e;
+                        if (i < count)
+                            for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], i, acc[e]);
+                    }
+                }
+            }
+        }
+    }
+    return true;
+}
+
+// Phase C for the packet write-backs: poll result packets of groups
+// [qb, qe) (step `stride`) and store their payload to outputs [j0, j1).
+template <int DT>
+__device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, size_t nbytes, size_t qb, size_t qe,
+                                               int j0, int j1, uint32_t epoch, uint64_t max_spins, int32_t* status,
+                                               bool out16, size_t tid, size_t stride) {
+    constexpr int EP = PerWord<DT>::kN;
+    const size_t npk = (nbytes + 3) / 4;
+    for (size_t q = qb + tid; q < qe; q += stride) {
+        if (16 * (q + 1) <= nbytes) {
+            uint64_t w[4];
+            ld_packets2(a.res + 4 * q, w[0], w[1]);
+            ld_packets2(a.res + 4 * q + 2, w[2], w[3]);
+            if (!poll<4>(a.res + 4 * q, epoch, max_spins, status, w)) return false;
+            const uint4 y = make_uint4(packet_payload(w[0]), packet_payload(w[1]), packet_payload(w[2]),
+                                       packet_payload(w[3]));
+            if (out16) {
+                for (int j = j0; j < j1; ++j) st_stream(static_cast<uint4*>(a.data.out[j]) + q, y);
+            } else {
+                const uint32_t words[4] = {y.x, y.y, y.z, y.w};
+                for (int j = j0; j < j1; ++j)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) store_bits<DT>(a.data.out[j], (4 * q + m) * EP + e, words[m], e);
+            }
+        } else {
+            const size_t wend = min(npk, 4 * q + 4);
+            for (size_t wi = 4 * q; wi < wend; ++wi) {
+                uint64_t pk[1] = {ld_packet(a.res + wi)};
+                if (!poll<1>(a.res + wi, epoch, max_spins, status, pk)) return false;
+                const uint32_t word = packet_payload(pk[0]);
+                for (int j = j0; j < j1; ++j)
+#pragma unroll
+                    for (int e = 0; e < EP; ++e)
+                        if (wi * EP + e < count) store_bits<DT>(a.data.out[j], wi * EP + e, word, e);
+            }
+        }
+    }
+    return true;
+}
+
+template <int DT, int NR, int WB>
+__global__ void __launch_bounds__(kThreads)
+coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t host_epoch,
+            uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16) {
+    __shared__ uint32_t s_epoch;
+    if (threadIdx.x == 0) {
+        uint32_t e = host_epoch;
+        if (ctrl != nullptr) {
+            e = ld_u32_v(ctrl) + 1;
+            if (e == 0) e = 1;
+        }
+        s_epoch = e;
+    }
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+    const int n = ranks<NR>(n_rt);
+    send(a, nbytes, epoch, in16, tid, stride);
+    bool ok = reduce<DT, NR, WB>(a, n_rt, count, nbytes, chunk_q, epoch, max_spins, status, out16, tid, stride);
+    if constexpr (WB == kPacketsAll) {
+        // Chunk (r + 1) mod N, reduced by other blocks: each result packet is
+        // read once and written to every output.
+        const size_t nq = ((nbytes + 3) / 4 + 3) / 4;
+        const size_t c = (static_cast<size_t>(blockIdx.y) + 1) % n;
+        const size_t qb = c * chunk_q, qe = min(nq, qb + chunk_q);
+        if (ok && qb < qe)
+            unpack_results<DT>(a, count, nbytes, qb, qe, 0, n, epoch, max_spins, status, out16, tid, stride);
+    } else if constexpr (WB == kPacketsOwn) {
+        // Rank j reads every result packet and writes its own output.
+        const size_t nq = ((nbytes + 3) / 4 + 3) / 4;
+        const int j = blockIdx.y;
+        if (ok) unpack_results<DT>(a, count, nbytes, 0, nq, j, j + 1, epoch, max_spins, status, out16, tid, stride);
+    }
+    if (ctrl != nullptr) {
+        // Every block read ctrl[0] before arriving; the last block to arrive
+        // publishes the epoch and resets the arrival count for the next launch.
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const uint32_t total = gridDim.x * gridDim.y;
+            if (atomicAdd(ctrl + 1, 1u) == total - 1) {
+                ctrl[1] = 0;
+                ctrl[0] = epoch;
+                __threadfence();
+            }
+        }
+    }
+}
+
+inline unsigned div_up(size_t a, size_t b) { return static_cast<unsigned>((a + b - 1) / b); }
+
+template <int DT, int NR, int WB>
+cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint32_t* ctrl,
+                          uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
+    const size_t nbytes = count * Elem<DT>::kSize;
+    const size_t npk = (nbytes + 3) / 4, nq = (npk + 3) / 4;
+    const size_t chunk_q = (nq + nranks - 1) / nranks;
+    // Blocks per rank: enough threads for the largest phase, capped so that
+    // all nranks * gx blocks are co-resident (resident blocks per SM x SMs,
+    // looked up once per device).
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> resident[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    int blocks = resident[dev].load(std::memory_order_relaxed);
+    if (blocks == 0) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, coop_kernel<DT, NR, WB>, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        blocks = sms * per_sm;
+        resident[dev].store(blocks, std::memory_order_relaxed);
+    }
+    size_t want = std::max<size_t>(div_up(npk, kThreads), div_up(chunk_q, kThreads));
+    if (WB == kPacketsOwn) want = std::max<size_t>(want, div_up(nq, kThreads));
+    const size_t cap = static_cast<size_t>(blocks) / nranks;
+    if (cap == 0) return cudaErrorCooperativeLaunchTooLarge;
+    const unsigned gx = static_cast<unsigned>(std::max<size_t>(1, std::min(want, cap)));
+    LLArgs args = a;
+    int n_rt = nranks;
+    size_t cnt = count, nb = nbytes, cq = chunk_q;
+    uint32_t ep = epoch;
+    uint32_t* ct = ctrl;
+    uint64_t ms = max_spins;
+    int32_t* st = status;
+    bool i16 = in16, o16 = out16;
+    void* params[] = {&args, &n_rt, &cnt, &nb, &cq, &ep, &ct, &ms, &st, &i16, &o16};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(coop_kernel<DT, NR, WB>), dim3(gx, nranks),
+                                       dim3(kThreads), params, 0, s);
+}
+
+template <int DT, int WB>
+cudaError_t coop_ranks(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint32_t* ctrl,
+                       uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
+    switch (nranks) {
+    case 1: return coop_dispatch<DT, 1, WB>(1, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 2: return coop_dispatch<DT, 2, WB>(2, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 4: return coop_dispatch<DT, 4, WB>(4, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 8: return coop_dispatch<DT, 8, WB>(8, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 16: return coop_dispatch<DT, 16, WB>(16, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 32: return coop_dispatch<DT, 32, WB>(32, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    default:
+        if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
+        return coop_dispatch<DT, 0, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    }
+}
+
+template <int WB>
+cudaError_t coop_launch(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, void* res, size_t count,
+                        uint32_t epoch, uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16,
+                        cudaStream_t stream) {
+    LLArgs a;
+    a.data = data;
+    for (int r = 0; r < SAR_MAX_RANKS; ++r) a.pkts[r] = r < nranks ? static_cast<uint64_t*>(pkts[r]) : nullptr;
+    a.res = static_cast<uint64_t*>(res);
+    switch (dt) {
+    case SAR_BF16: return coop_ranks<SAR_BF16, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    case SAR_FP16: return coop_ranks<SAR_FP16, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    case SAR_FP32: return coop_ranks<SAR_FP32, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    case SAR_FP8_E4M3FN:
+        return coop_ranks<SAR_FP8_E4M3FN, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    case SAR_FP8_E4M3B15:
+        return coop_ranks<SAR_FP8_E4M3B15, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace llc
+}  // namespace sar

@@ -52,7 +52,7 @@ cudaError_t scratch_base(int dev, unsigned char** out) {
     return d.err;
 }
 
-bool supported(int n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32; }
+bool supported(int n) { return n >= 1 && n <= SAR_MAX_RANKS; }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -65,7 +65,7 @@ extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, vo
                                                        size_t count, sar_dtype dtype, uint64_t max_spins,
                                                        int32_t* d_status, sar_stream_t stream) {
     if (!supported(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
-    if (dtype < SAR_BF16 || dtype > SAR_FP8_E4M3FN) return SAR_ERR_UNSUPPORTED_DTYPE;
+    if (dtype < SAR_BF16 || dtype > SAR_FP8_E4M3B15) return SAR_ERR_UNSUPPORTED_DTYPE;
     if (in == nullptr || out == nullptr || max_spins == 0) return SAR_ERR_INVALID_ARG;
     const size_t es = esize_of(dtype);
     if (count > (SIZE_MAX / 16) / es) return SAR_ERR_INVALID_ARG;

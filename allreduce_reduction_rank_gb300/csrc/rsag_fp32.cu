@@ -1,0 +1,8 @@
+// rsag_fp32.cu -- the rsag reduce kernels for fp32 elements with a binary32
+// accumulator (one translation unit per element type and accumulator group
+// keeps the parallel build short).
+#include "rsag_kernels.cuh"
+
+namespace sar {
+template cudaError_t launch_rsag_wide<SAR_FP32>(RsagMode, int, const RankPtrs&, size_t, size_t, bool, cudaStream_t);
+}  // namespace sar

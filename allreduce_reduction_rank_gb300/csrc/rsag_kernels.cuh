@@ -1,0 +1,265 @@
+// rsag_kernels.cuh -- the rsag reduce kernels for every accumulator type,
+// instantiated per element type by the small rsag_<type>.cu (binary32
+// accumulator) and rsag_<type>_acc.cu (narrower accumulators) files.
+//
+// "Support 2 ranks in AllreduceRsAgZeroCopy - #948" ("what changed"): the rsag
+// zero-copy kernel is generic in NRanks, NPeers = NRanks - 1, with the peer
+// loops unrolled at compile time; each rank reads its 1/N chunk from every
+// peer's input, reduces it and writes it into every peer's output.  Here the
+// N ranks are N buffers in this GPU's HBM and rank r is the blockIdx.y slice
+// of the grid, so the same structure becomes one streaming kernel:
+//
+//   per thread and 16-byte vector:  N loads -> sum in rank order -> one
+//                                   rounding -> N stores
+//
+// HBM traffic is the algorithmic minimum, N*S read + N*S written.  NRanks is a
+// template parameter, so the rank loops are fully unrolled and every load of
+// a tile is issued before the first add.
+//
+// ACC is the accumulator type (mscclpp commit history, "Add mixed-precision
+// accumulation for allreduce": accumDtype).  With ACC = binary32 the partial
+// sums are exact binary32 adds; with a narrower ACC every partial sum is
+// rounded into ACC: acc_0 = R_acc(x_0), acc_k = R_acc(acc_{k-1} + x_k).
+#pragma once
+
+#include "sar_device.cuh"
+#include "sar_internal.h"
+
+namespace sar {
+namespace rsag {
+
+// Loads in flight per thread: all ranks for up to 8 ranks (x UNROLL vectors),
+// windows of 8 ranks above that to bound register use.  NR = 0 is the kernel
+// for a rank count known only at run time (any count up to SAR_MAX_RANKS):
+// windows of 4 predicated loads.
+template <int NR> struct Shape {
+    static constexpr int kWin = NR < 8 ? NR : 8;
+    static constexpr int kUnroll = NR <= 2 ? 4 : (NR <= 8 ? 2 : 1);
+};
+template <> struct Shape<0> {
+    static constexpr int kWin = 4;
+    static constexpr int kUnroll = 2;
+};
+
+// x -> R_acc(x) as a binary32 value.
+template <int ACC> __device__ __forceinline__ float round_acc(float x);
+template <> __device__ __forceinline__ float round_acc<SAR_FP32>(float x) { return x; }
+template <> __device__ __forceinline__ float round_acc<SAR_FP16>(float x) {
+    return __half2float(__float2half_rn(x));
+}
+template <> __device__ __forceinline__ float round_acc<SAR_BF16>(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+template <> __device__ __forceinline__ float round_acc<SAR_FP8_E4M3FN>(float x) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3), __NV_E4M3);
+    return __half2float(*reinterpret_cast<__half*>(&h));
+}
+
+template <> __device__ __forceinline__ float round_acc<SAR_FP8_E4M3B15>(float x) {
+    return e4m3b15_to_f32(f32_to_e4m3b15(x));
+}
+
+template <int DT, int ACC> __device__ __forceinline__ void seed(Acc<DT>& a, const uint4& v) {
+    acc_seed<DT>(a, v);
+    if constexpr (ACC != SAR_FP32) {
+#pragma unroll
+        for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+    }
+}
+
+template <int DT, int ACC> __device__ __forceinline__ void add(Acc<DT>& a, const uint4& v) {
+    acc_add<DT>(a, v);
+    if constexpr (ACC != SAR_FP32) {
+#pragma unroll
+        for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+    }
+}
+
+template <int MODE, int NR>
+__device__ __forceinline__ void store_vector(const RankPtrs& p, int n_rt, int r, size_t v, const uint4& y) {
+    if (MODE == kFused) {
+#pragma unroll
+        for (int j = 0; j < ranks<NR>(n_rt); ++j) st_stream(static_cast<uint4*>(p.out[j]) + v, y);
+    } else {
+        st_stream(static_cast<uint4*>(p.out[r]) + v, y);
+    }
+}
+
+template <int DT, int NR, int MODE, int ACC>
+__device__ __forceinline__ void reduce_element(const RankPtrs& p, int n_rt, int r, size_t i) {
+    float acc = round_acc<ACC>(load_elem<DT>(p.in[0], i));
+#pragma unroll
+    for (int k = 1; k < ranks<NR>(n_rt); ++k) acc = round_acc<ACC>(__fadd_rn(acc, load_elem<DT>(p.in[k], i)));
+    if (MODE == kFused) {
+#pragma unroll
+        for (int j = 0; j < ranks<NR>(n_rt); ++j) store_elem<DT>(p.out[j], i, acc);
+    } else {
+        store_elem<DT>(p.out[r], i, acc);
+    }
+}
+
+// Ranks [k0, k0 + WIN) of vectors v[0..U): loads first, then the in-order adds
+// (the first rank seeds the accumulator).  With NR == 0 the ranks at or past
+// n_rt are skipped.
+template <int DT, int NR, int ACC, int WIN, int U>
+__device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k0, const size_t (&v)[U],
+                                              Acc<DT> (&acc)[U]) {
+    uint4 x[WIN][U];
+#pragma unroll
+    for (int k = 0; k < WIN; ++k)
+        if (NR > 0 || k0 + k < n_rt)
+#pragma unroll
+            for (int u = 0; u < U; ++u) x[k][u] = ld_stream(static_cast<const uint4*>(p.in[k0 + k]) + v[u]);
+#pragma unroll
+    for (int k = 0; k < WIN; ++k)
+        if (NR > 0 || k0 + k < n_rt)
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (k0 + k == 0) seed<DT, ACC>(acc[u], x[k][u]);
+                else add<DT, ACC>(acc[u], x[k][u]);
+            }
+}
+
+// One full 16-byte vector (index v counted from the start of the buffers).
+template <int DT, int NR, int MODE, int ACC>
+__device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r, size_t v) {
+    constexpr int WIN = Shape<NR>::kWin;
+    Acc<DT> acc[1];
+    const size_t vv[1] = {v};
+#pragma unroll 1
+    for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, 1>(p, n_rt, k0, vv, acc);
+    store_vector<MODE, NR>(p, n_rt, r, v, acc_round<DT>(acc[0]));
+}
+
+// Vector kernel: grid = (tiles of chunk r, nranks).  Requires every buffer to
+// be 16-byte aligned; chunk is a multiple of the vector length.
+template <int DT, int NR, int MODE, int ACC>
+__global__ void __launch_bounds__(kThreads)
+vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
+    constexpr int VE = Elem<DT>::kVE;
+    constexpr int WIN = Shape<NR>::kWin;
+    constexpr int UNROLL = Shape<NR>::kUnroll;
+    const int r = blockIdx.y;
+    const size_t begin = static_cast<size_t>(r) * chunk;
+    if (begin >= count) return;
+    const size_t end = min(count, begin + chunk);
+    const size_t vbase = begin / VE;
+    const size_t nfull = (end - begin) / VE;            // whole vectors in the chunk
+    const size_t nvec = (end - begin + VE - 1) / VE;    // plus a partial one at the very end
+    const size_t tile = static_cast<size_t>(kThreads) * UNROLL;
+
+    for (size_t t0 = static_cast<size_t>(blockIdx.x) * tile; t0 < nvec;
+         t0 += static_cast<size_t>(gridDim.x) * tile) {
+        if (t0 + tile <= nfull) {
+            // Interior tile: UNROLL vectors per thread, all loads of a rank
+            // window issued before the first add.
+            size_t v[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) v[u] = vbase + t0 + u * kThreads + threadIdx.x;
+            Acc<DT> acc[UNROLL];
+            // Windows of 8 ranks run as a loop (one window for up to 8 ranks).
+#pragma unroll 1
+            for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, UNROLL>(p, n_rt, k0, v, acc);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) store_vector<MODE, NR>(p, n_rt, r, v[u], acc_round<DT>(acc[u]));
+        } else {
+            // Edge tile: whole vectors one at a time, then the partial vector
+            // (only the last chunk can end inside a vector) element by element.
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const size_t v = t0 + u * kThreads + threadIdx.x;
+                if (v < nfull) {
+                    reduce_vector<DT, NR, MODE, ACC>(p, n_rt, r, vbase + v);
+                } else if (v < nvec) {
+                    for (size_t i = begin + v * VE; i < end; ++i) reduce_element<DT, NR, MODE, ACC>(p, n_rt, r, i);
+                }
+            }
+        }
+    }
+}
+
+// Element kernel for buffers that are not all 16-byte aligned (the slow
+// path): the rank loop runs to the runtime nranks, so one instantiation
+// serves every rank count.
+template <int DT, int MODE, int ACC>
+__global__ void __launch_bounds__(kThreads)
+scalar_kernel(const RankPtrs p, int nranks, size_t count, size_t chunk) {
+    const int r = blockIdx.y;
+    const size_t begin = static_cast<size_t>(r) * chunk;
+    if (begin >= count) return;
+    const size_t end = min(count, begin + chunk);
+    for (size_t i = begin + static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; i < end;
+         i += static_cast<size_t>(gridDim.x) * kThreads)
+        reduce_element<DT, 0, MODE, ACC>(p, nranks, r, i);
+}
+
+inline unsigned grid_x(size_t items, size_t per_cta, size_t cap) {
+    size_t g = (items + per_cta - 1) / per_cta;
+    if (g < 1) g = 1;
+    if (g > cap) g = cap;
+    return static_cast<unsigned>(g);
+}
+
+constexpr size_t kMaxGridX = 0x7FFFFFFF;
+constexpr size_t kScalarGridX = 8192;
+
+template <int DT, int NR, int MODE, int ACC>
+cudaError_t launch_vec(const RankPtrs& p, int nranks, size_t count, size_t chunk, cudaStream_t s) {
+    constexpr int VE = Elem<DT>::kVE;
+    const size_t tile = static_cast<size_t>(kThreads) * Shape<NR>::kUnroll;
+    const dim3 grid(grid_x((chunk + VE - 1) / VE, tile, kMaxGridX), nranks);
+    vec_kernel<DT, NR, MODE, ACC><<<grid, kThreads, 0, s>>>(p, nranks, count, chunk);
+    return cudaGetLastError();
+}
+
+template <int DT, int MODE, int ACC>
+cudaError_t launch_ranks(int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec, cudaStream_t s) {
+    if (!vec) {
+        const dim3 grid(grid_x(chunk, kThreads, kScalarGridX), nranks);
+        scalar_kernel<DT, MODE, ACC><<<grid, kThreads, 0, s>>>(p, nranks, count, chunk);
+        return cudaGetLastError();
+    }
+    switch (nranks) {
+    case 1: return launch_vec<DT, 1, MODE, ACC>(p, 1, count, chunk, s);
+    case 2: return launch_vec<DT, 2, MODE, ACC>(p, 2, count, chunk, s);
+    case 4: return launch_vec<DT, 4, MODE, ACC>(p, 4, count, chunk, s);
+    case 8: return launch_vec<DT, 8, MODE, ACC>(p, 8, count, chunk, s);
+    case 16: return launch_vec<DT, 16, MODE, ACC>(p, 16, count, chunk, s);
+    case 32: return launch_vec<DT, 32, MODE, ACC>(p, 32, count, chunk, s);
+    default:
+        if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
+        return launch_vec<DT, 0, MODE, ACC>(p, nranks, count, chunk, s);   // any other count
+    }
+}
+
+}  // namespace rsag
+
+// The reduce launchers of one element type: binary32 accumulation in either
+// mode (instantiated in rsag_<type>.cu), and fp16, bf16 or, for FP8 types,
+// native accumulation in the fused mode (instantiated in rsag_<type>_acc.cu).
+template <int DT>
+cudaError_t launch_rsag_wide(RsagMode mode, int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec,
+                             cudaStream_t s) {
+    if (mode == kFused) return rsag::launch_ranks<DT, kFused, SAR_FP32>(nranks, p, count, chunk, vec, s);
+    return rsag::launch_ranks<DT, kReduceScatter, SAR_FP32>(nranks, p, count, chunk, vec, s);
+}
+
+template <int DT>
+cudaError_t launch_rsag_narrow(sar_dtype acc, int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec,
+                               cudaStream_t s) {
+    switch (acc) {
+    case SAR_FP16: return rsag::launch_ranks<DT, kFused, SAR_FP16>(nranks, p, count, chunk, vec, s);
+    case SAR_BF16: return rsag::launch_ranks<DT, kFused, SAR_BF16>(nranks, p, count, chunk, vec, s);
+    case SAR_FP8_E4M3FN:
+        if constexpr (DT == SAR_FP8_E4M3FN)
+            return rsag::launch_ranks<DT, kFused, SAR_FP8_E4M3FN>(nranks, p, count, chunk, vec, s);
+        return cudaErrorInvalidValue;
+    case SAR_FP8_E4M3B15:
+        if constexpr (DT == SAR_FP8_E4M3B15)
+            return rsag::launch_ranks<DT, kFused, SAR_FP8_E4M3B15>(nranks, p, count, chunk, vec, s);
+        return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sar

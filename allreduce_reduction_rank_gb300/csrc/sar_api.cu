@@ -5,8 +5,9 @@
 // "Support 2 ranks in AllreduceRsAgZeroCopy - #948" ("why") an unsupported
 // rank count made the adapter return an error without launching, which the
 // NCCL shim surfaced as ncclInvalidArgument; here the same condition is an
-// explicit SAR_ERR_UNSUPPORTED_NRANKS, and the supported set is the #948 set
-// {2, 4, 8, 16, 32} plus the trivial single rank.
+// explicit SAR_ERR_UNSUPPORTED_NRANKS.  The #948 set {2, 4, 8, 16, 32} (plus
+// the trivial single rank) has compile-time-unrolled kernels; the counts that
+// #948 still rejects (3, 5, 6, 7, ...) run kernels with a runtime rank loop.
 #include <cstdint>
 #include <cstring>
 
@@ -20,15 +21,21 @@ size_t esize_of(sar_dtype dt) {
     case SAR_FP16: return 2;
     case SAR_FP32: return 4;
     case SAR_FP8_E4M3FN: return 1;
+    case SAR_FP8_E4M3B15: return 1;
     }
     return 0;
 }
 
 namespace {
 
-bool supported_nranks(int n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32; }
+// Any count from 1 to SAR_MAX_RANKS: 1, 2, 4, 8, 16 and 32 run kernels with the
+// rank loops unrolled at compile time, every other count a kernel that loops
+// over the ranks at run time (same order, same results).
+bool supported_nranks(int n) { return n >= 1 && n <= SAR_MAX_RANKS; }
 
-bool valid_dtype(int dt) { return dt >= SAR_BF16 && dt <= SAR_FP8_E4M3FN; }
+bool valid_dtype(int dt) { return dt >= SAR_BF16 && dt <= SAR_FP8_E4M3B15; }
+
+bool is_fp8(int dt) { return dt == SAR_FP8_E4M3FN || dt == SAR_FP8_E4M3B15; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -140,6 +147,21 @@ SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nr
     return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), chunk, vec, s));
 }
 
+SAR_API sar_status sar_allreduce_accum(const void* const* in, void* const* out, int nranks, size_t count,
+                                       sar_dtype dtype, sar_dtype accum, sar_stream_t stream) {
+    if (!valid_dtype(accum)) return SAR_ERR_UNSUPPORTED_DTYPE;
+    const bool narrow = accum == SAR_FP16 || accum == SAR_BF16 || (accum == dtype);
+    if (accum != SAR_FP32 && !narrow) return SAR_ERR_UNSUPPORTED_DTYPE;
+    RankPtrs p;
+    bool vec = false, launch = false;
+    sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
+    if (st != SAR_OK || !launch) return st;
+    const size_t chunk = rsag_chunk(count, nranks, dtype);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (accum == SAR_FP32) return to_status(launch_rsag(kFused, dtype, nranks, p, count, chunk, vec, s));
+    return to_status(launch_rsag_accum(dtype, accum, nranks, p, count, chunk, vec, s));
+}
+
 SAR_API sar_status sar_reduce_scatter(const void* const* in, void* const* out, int nranks, size_t count,
                                       sar_dtype dtype, sar_stream_t stream) {
     RankPtrs p;
@@ -225,10 +247,58 @@ SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, voi
     return to_status(launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, s));
 }
 
+SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                                          size_t count, sar_dtype dtype, uint32_t epoch, uint32_t* d_epoch,
+                                          uint64_t max_spins, int32_t* d_status, sar_stream_t stream) {
+    bool launch = false, in16 = false, out16 = false;
+    // With a device epoch counter the host epoch is unused; any non-zero value
+    // passes the shared check.
+    sar_status st = check_ll(in, pkts, nranks, count, dtype, d_epoch != nullptr ? 1u : epoch, &launch, &in16);
+    if (st != SAR_OK) return st;
+    if (out == nullptr) return SAR_ERR_INVALID_ARG;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (d_epoch != nullptr && !aligned(d_epoch, 8)) return SAR_ERR_MISALIGNED;
+    if (!launch) return SAR_OK;
+    if ((st = check_ll(out, pkts, nranks, count, dtype, 1u, &launch, &out16)) != SAR_OK) return st;
+    RankPtrs data;
+    std::memset(&data, 0, sizeof(data));
+    for (int r = 0; r < nranks; ++r) {
+        data.in[r] = in[r];
+        data.out[r] = out[r];
+    }
+    return to_status(launch_ll_fused(dtype, nranks, data, pkts, count, epoch, d_epoch, max_spins, d_status, in16,
+                                     out16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const* out, void* const* pkts, void* res,
+                                              int nranks, size_t count, sar_dtype dtype, uint32_t epoch,
+                                              uint32_t* d_epoch, int multi_dest, uint64_t max_spins,
+                                              int32_t* d_status, sar_stream_t stream) {
+    bool launch = false, in16 = false, out16 = false;
+    sar_status st = check_ll(in, pkts, nranks, count, dtype, d_epoch != nullptr ? 1u : epoch, &launch, &in16);
+    if (st != SAR_OK) return st;
+    if (out == nullptr) return SAR_ERR_INVALID_ARG;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (d_epoch != nullptr && !aligned(d_epoch, 8)) return SAR_ERR_MISALIGNED;
+    if (!launch) return SAR_OK;
+    if (res == nullptr) return SAR_ERR_INVALID_ARG;
+    if (!aligned(res, 16)) return SAR_ERR_MISALIGNED;
+    if ((st = check_ll(out, pkts, nranks, count, dtype, 1u, &launch, &out16)) != SAR_OK) return st;
+    RankPtrs data;
+    std::memset(&data, 0, sizeof(data));
+    for (int r = 0; r < nranks; ++r) {
+        data.in[r] = in[r];
+        data.out[r] = out[r];
+    }
+    return to_status(launch_ll_writeback(dtype, nranks, data, pkts, res, count, epoch, d_epoch, multi_dest != 0,
+                                         max_spins, d_status, in16, out16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 SAR_API sar_status sar_fp8_convert(const void* src, sar_dtype src_dtype, void* dst, sar_dtype dst_dtype,
                                    size_t count, sar_stream_t stream) {
     if (!valid_dtype(src_dtype) || !valid_dtype(dst_dtype)) return SAR_ERR_UNSUPPORTED_DTYPE;
-    const bool pair_ok = (src_dtype == SAR_FP8_E4M3FN) != (dst_dtype == SAR_FP8_E4M3FN);
+    // One side FP8, the other fp32, fp16 or bf16.
+    const bool pair_ok = is_fp8(src_dtype) != is_fp8(dst_dtype);
     if (!pair_ok) return SAR_ERR_UNSUPPORTED_DTYPE;
     if (src == nullptr || dst == nullptr) return SAR_ERR_INVALID_ARG;
     const size_t ses = esize_of(src_dtype), des = esize_of(dst_dtype);
@@ -256,7 +326,7 @@ SAR_API const char* sar_status_string(sar_status status) {
     switch (status) {
     case SAR_OK: return "SAR_OK";
     case SAR_ERR_INVALID_ARG: return "SAR_ERR_INVALID_ARG: invalid argument";
-    case SAR_ERR_UNSUPPORTED_NRANKS: return "SAR_ERR_UNSUPPORTED_NRANKS: nranks must be 1, 2, 4, 8, 16 or 32";
+    case SAR_ERR_UNSUPPORTED_NRANKS: return "SAR_ERR_UNSUPPORTED_NRANKS: nranks must be between 1 and 32";
     case SAR_ERR_UNSUPPORTED_DTYPE: return "SAR_ERR_UNSUPPORTED_DTYPE: unsupported element type or conversion";
     case SAR_ERR_MISALIGNED: return "SAR_ERR_MISALIGNED: buffer not aligned to its element (packets: 16 bytes)";
     case SAR_ERR_CUDA: return "SAR_ERR_CUDA: a CUDA launch or copy failed";

@@ -24,6 +24,11 @@ namespace sar {
 
 constexpr int kThreads = 256;
 
+// Kernels take the rank count as a template parameter NR, unrolled at compile
+// time for 1, 2, 4, 8, 16 and 32 ranks; NR == 0 is the variant for any other
+// count, passed at run time.
+template <int NR> __device__ __forceinline__ int ranks(int n_rt) { return NR > 0 ? NR : n_rt; }
+
 // ---------------------------------------------------------------------------
 // Element types.  kVE = elements per 16-byte vector.
 // ---------------------------------------------------------------------------
@@ -32,6 +37,36 @@ template <> struct Elem<SAR_BF16> { static constexpr int kSize = 2, kVE = 8; };
 template <> struct Elem<SAR_FP16> { static constexpr int kSize = 2, kVE = 8; };
 template <> struct Elem<SAR_FP32> { static constexpr int kSize = 4, kVE = 4; };
 template <> struct Elem<SAR_FP8_E4M3FN> { static constexpr int kSize = 1, kVE = 16; };
+template <> struct Elem<SAR_FP8_E4M3B15> { static constexpr int kSize = 1, kVE = 16; };
+
+// e4m3b15 (1 sign, 4 exponent with bias 15, 3 fraction bits; exponent field
+// 15 = infinity / NaN) has no hardware conversion; these follow the format's
+// definition.  Widening places the 7 magnitude bits under the binary32
+// exponent field, which reads them with bias 127, and rescales by 2^(127-15):
+// exact for normals and subnormals alike.
+__device__ __forceinline__ float e4m3b15_to_f32(uint32_t b) {
+    const uint32_t em = b & 0x7Fu, sign = (b & 0x80u) << 24;
+    const float finite = __uint_as_float(sign | (em << 20)) * 0x1p112f;
+    const uint32_t special = em == 0x78u ? (sign | 0x7F800000u) : 0x7FFFFFFFu;   // inf or NaN
+    return em >= 0x78u ? __uint_as_float(special) : finite;
+}
+
+// Narrowing: round to nearest even, overflow (|x| >= 0.96875, the midpoint
+// above 0.9375) to infinity, NaN to 0x7F.  Branch-free: every candidate is
+// computed and the right one selected.
+__device__ __forceinline__ uint32_t f32_to_e4m3b15(float x) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t sign = (u >> 24) & 0x80u, a = u & 0x7FFFFFFFu;
+    // |x| < 2^-14: the subnormal grid of 2^-17 (exact scaling, then RNE).
+    const uint32_t sub = __float2uint_rn(__uint_as_float(a) * 0x1p17f);
+    // Normal: keep 3 fraction bits, ties to even; a carry moves into the
+    // exponent.  Exponent fields differ by 127 - 15 = 112.
+    const uint32_t r = a + 0x7FFFFu + ((a >> 20) & 1u);
+    const uint32_t norm = (r >> 20) - (112u << 3);
+    uint32_t m = a < 0x38800000u ? sub : norm;
+    m = a >= 0x3F780000u ? 0x78u : m;                          // >= 0.96875: infinity
+    return a > 0x7F800000u ? 0x7Fu : (sign | m);
+}
 
 // Exact widening of one 32-bit word holding 2 (16-bit types), 1 (fp32) or
 // 4 (e4m3fn) elements, lowest address first.
@@ -76,6 +111,38 @@ template <> __device__ __forceinline__ uint32_t narrow_word<SAR_FP8_E4M3FN>(cons
     uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);
     uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[2], x[3]), __NV_SATFINITE, __NV_E4M3);
     return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Four codes one at a time (the rare words holding an infinity or NaN code);
+// kept out of line so the unrolled reduction loops stay small.
+static __device__ __noinline__ float4 e4m3b15_word_exact(uint32_t w) {
+    return make_float4(e4m3b15_to_f32(w & 0xFFu), e4m3b15_to_f32((w >> 8) & 0xFFu),
+                       e4m3b15_to_f32((w >> 16) & 0xFFu), e4m3b15_to_f32(w >> 24));
+}
+
+// e4m3b15 and binary16 share the bias 15, so a finite e4m3b15 code is the top
+// of a binary16: sign to bit 15, exponent and fraction to bits 7..13.  Two
+// codes become one f16x2 with a byte permute and two bit operations, then the
+// hardware widens f16 -> f32 (exact).  Codes with exponent field 15 (infinity
+// and NaN, which binary16 would read as 1.0 .. 1.875) take the per-code path;
+// a SWAR test finds them: (code & 0x7F) + 8 carries into bit 7 exactly when
+// the code's exponent field is 15.
+template <> __device__ __forceinline__ void widen_word<SAR_FP8_E4M3B15>(uint32_t w, float* x) {
+    if ((((w & 0x7F7F7F7Fu) + 0x08080808u) & 0x80808080u) == 0u) {
+        const uint32_t b01 = __byte_perm(w, 0u, 0x1404), b23 = __byte_perm(w, 0u, 0x3424);   // [0,b0,0,b1], [0,b2,0,b3]
+        uint32_t h01 = (b01 & 0x80008000u) | ((b01 & 0x7F007F00u) >> 1);
+        uint32_t h23 = (b23 & 0x80008000u) | ((b23 & 0x7F007F00u) >> 1);
+        const float2 f01 = __half22float2(*reinterpret_cast<__half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<__half2*>(&h23));
+        x[0] = f01.x; x[1] = f01.y; x[2] = f23.x; x[3] = f23.y;
+    } else {
+        const float4 f = e4m3b15_word_exact(w);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    }
+}
+template <> __device__ __forceinline__ uint32_t narrow_word<SAR_FP8_E4M3B15>(const float* x) {
+    return f32_to_e4m3b15(x[0]) | (f32_to_e4m3b15(x[1]) << 8) | (f32_to_e4m3b15(x[2]) << 16) |
+           (f32_to_e4m3b15(x[3]) << 24);
 }
 
 // Elements per 32-bit word.
@@ -136,6 +203,10 @@ template <> __device__ __forceinline__ float load_elem<SAR_FP8_E4M3FN>(const voi
     return __half2float(*reinterpret_cast<__half*>(&h));
 }
 
+template <> __device__ __forceinline__ float load_elem<SAR_FP8_E4M3B15>(const void* base, size_t i) {
+    return e4m3b15_to_f32(static_cast<const unsigned char*>(base)[i]);
+}
+
 template <int DT> __device__ __forceinline__ void store_elem(void* base, size_t i, float x);
 template <> __device__ __forceinline__ void store_elem<SAR_BF16>(void* base, size_t i, float x) {
     static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
@@ -148,6 +219,10 @@ template <> __device__ __forceinline__ void store_elem<SAR_FP32>(void* base, siz
 }
 template <> __device__ __forceinline__ void store_elem<SAR_FP8_E4M3FN>(void* base, size_t i, float x) {
     static_cast<__nv_fp8_storage_t*>(base)[i] = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+template <> __device__ __forceinline__ void store_elem<SAR_FP8_E4M3B15>(void* base, size_t i, float x) {
+    static_cast<unsigned char*>(base)[i] = static_cast<unsigned char>(f32_to_e4m3b15(x));
 }
 
 // Widen element `e` of a 32-bit payload word (used by the LL tail).

@@ -25,6 +25,21 @@ struct RankPtrs {
 cudaError_t launch_rsag(RsagMode mode, sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
                         size_t chunk, bool vec, cudaStream_t stream);
 
+// Fused rsag allreduce with partial sums rounded into `acc` (fp16, bf16, or
+// e4m3fn for e4m3fn inputs).
+cudaError_t launch_rsag_accum(sar_dtype dt, sar_dtype acc, int nranks, const RankPtrs& p, size_t count,
+                              size_t chunk, bool vec, cudaStream_t stream);
+
+// The reduce launchers of one element type (rsag_kernels.cuh): binary32
+// accumulation in either mode (instantiated in rsag_<type>.cu), and fp16 /
+// bf16 / native FP8 accumulation in the fused mode (rsag_<type>_acc.cu).
+template <int DT>
+cudaError_t launch_rsag_wide(RsagMode mode, int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec,
+                             cudaStream_t s);
+template <int DT>
+cudaError_t launch_rsag_narrow(sar_dtype acc, int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec,
+                               cudaStream_t s);
+
 // rsag all-gather: out[j][chunk r] = out[r][chunk r], j != r (bytes).
 cudaError_t launch_all_gather(int nranks, const RankPtrs& p, size_t count, size_t esize,
                               size_t chunk, bool vec, cudaStream_t stream);
@@ -37,6 +52,18 @@ cudaError_t launch_ll_pack(int nranks, const RankPtrs& p, size_t bytes, uint32_t
 cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
                                     uint32_t epoch, uint64_t max_spins, int32_t* status,
                                     bool vec_out, cudaStream_t stream);
+
+// LL send + reduce + write-back in one cooperative launch.  ctrl: optional
+// device {last epoch, arrivals}; with it the epoch is ctrl[0] + 1.
+cudaError_t launch_ll_fused(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, size_t count,
+                            uint32_t epoch, uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16,
+                            bool out16, cudaStream_t stream);
+
+// LL with the write-back as a second packet round into `res`; multi_dest:
+// each result packet is read once and written to all outputs.
+cudaError_t launch_ll_writeback(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, void* res,
+                                size_t count, uint32_t epoch, uint32_t* ctrl, bool multi_dest, uint64_t max_spins,
+                                int32_t* status, bool in16, bool out16, cudaStream_t stream);
 
 cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
                            size_t count, bool vec, cudaStream_t stream);

@@ -43,10 +43,13 @@ GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic of one launch of the dominant kernel (rsag fused, fp16, 8 ranks,
-# 64 MiB per rank) from one ncu capture, valid while the kernel sources hash to
-# `sources_sha`; otherwise `traffic` is reported as null.
-TRAFFIC = {"sources_sha": None, "bytes_per_launch": None}
-KERNEL_SOURCES = ["allreduce_reduction_rank_gb300/csrc/rsag.cu",
+# 64 MiB per rank) from one ncu capture (dram__bytes_read.sum 536,978,432 +
+# dram__bytes_write.sum 487,227,648; the rest of the 536.9 MB of outputs is
+# still dirty in L2 when the launch ends), valid while the kernel sources hash
+# to `sources_sha`; otherwise `traffic` is reported as null.
+TRAFFIC = {"sources_sha": "48e7ed87f073df85", "bytes_per_launch": 1024206080}
+KERNEL_SOURCES = ["allreduce_reduction_rank_gb300/csrc/rsag_kernels.cuh",
+                  "allreduce_reduction_rank_gb300/csrc/rsag_fp16.cu",
                   "allreduce_reduction_rank_gb300/csrc/sar_device.cuh"]
 
 
@@ -159,8 +162,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # The GPU arm.
 # ---------------------------------------------------------------------------
-TORCH_STORAGE = {"bf16": "int16", "fp16": "int16", "fp32": "float32", "e4m3fn": "uint8"}
-NP_VIEW = {"bf16": np.int16, "fp16": np.int16, "fp32": np.float32, "e4m3fn": np.uint8}
+NP_VIEW = {"bf16": np.int16, "fp16": np.int16, "fp32": np.float32, "e4m3fn": np.uint8, "e4m3b15": np.uint8}
 
 
 def upload(torch, codes, dt, dev):
@@ -196,21 +198,25 @@ def time_graph(torch, fn, calls: int, stream) -> float:
     return start.elapsed_time(end) / calls
 
 
-def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, graph=True, ins=None):
+def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, graph=True, ins=None, accum=None):
     ins = ins if ins is not None else wl.inputs()
     din = [upload(torch, x, wl.dtype, dev) for x in ins]
     dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
     pi, po = [t.data_ptr() for t in din], [t.data_ptr() for t in dout]
 
     def call():
-        sar.sar_allreduce(pi, po, count=wl.count, dtype=wl.dtype, algo=algo, stream=stream.cuda_stream)
+        if accum is None:
+            sar.sar_allreduce(pi, po, count=wl.count, dtype=wl.dtype, algo=algo, stream=stream.cuda_stream)
+        else:
+            sar.sar_allreduce_accum(pi, po, accum, count=wl.count, dtype=wl.dtype, stream=stream.cuda_stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warm):
             call()
         eager = time_calls(torch, call, calls, stream)
         g = time_graph(torch, call, calls, stream) if graph else None
-    row = {"workload": wl.name, "algo": ["rsag", "rsag_two_phase"][algo], "bytes": wl.algo_bytes,
+    name = ["rsag", "rsag_two_phase"][algo] if accum is None else f"rsag, {accum} accumulation"
+    row = {"workload": wl.name, "algo": name, "bytes": wl.algo_bytes,
            "eager_us": round(eager * 1e3, 3), "eager_GBps": round(wl.algo_bytes / (eager * 1e-3) / GB, 1),
            "l2_resident": wl.algo_bytes <= l2_bytes}
     if g is not None:
@@ -237,11 +243,87 @@ def ll_row(torch, sar, wl, dev, stream, calls):
 
     with torch.cuda.stream(stream):
         ms = time_calls(torch, call, calls, stream)
+        # CUDA graph: `calls` calls with epochs calls+1 .. 2*calls captured once;
+        # a replay re-packs every packet before it is polled, so replays are safe.
+        g_ms = time_graph(torch, call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
     phys = 6 * wl.nranks * wl.bytes_per_rank
     return {"workload": wl.name, "calls": calls, "epochs": f"1..{calls}", "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
-            "physical_GBps": round(phys / (ms * 1e-3) / GB, 2), "status_ok": ok}
+            "physical_GBps": round(phys / (ms * 1e-3) / GB, 2),
+            "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
+            "status_ok": ok}
+
+
+def ll_fused_row(torch, sar, wl, dev, stream, calls):
+    """LL in one cooperative launch: eager with host epochs 1..calls, and a
+    CUDA graph of `calls` launches that take their epochs from the device
+    control block (so every replay continues the epoch sequence)."""
+    ins = wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    pk = [torch.zeros(sar.sar_ll_packet_bytes(wl.count, wl.dtype), dtype=torch.uint8, device=dev)
+          for _ in range(wl.nranks)]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ctrl = torch.zeros(2, dtype=torch.int32, device=dev)
+    pi, po, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in dout], [t.data_ptr() for t in pk]
+    epoch = [0]
+
+    def host_epoch_call():
+        epoch[0] += 1
+        sar.sar_allreduce_ll_fused(pi, po, pp, st.data_ptr(), epoch=epoch[0], count=wl.count, dtype=wl.dtype,
+                                   stream=stream.cuda_stream)
+
+    def device_epoch_call():
+        sar.sar_allreduce_ll_fused(pi, po, pp, st.data_ptr(), epoch_ctrl=ctrl.data_ptr(), count=wl.count,
+                                   dtype=wl.dtype, stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_calls(torch, host_epoch_call, calls, stream)
+        # continue the epoch sequence on the device after the host epochs
+        ctrl[0] = epoch[0]
+        g_ms = time_graph(torch, device_epoch_call, calls, stream)
+    ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    return {"workload": wl.name + "_fused", "calls": calls, "us_per_call": round(ms * 1e3, 3),
+            "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
+            "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
+            "epochs_on_device": int(ctrl[0].item()), "status_ok": ok}
+
+
+def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
+    """LL with the write-back as a second packet round (one cooperative
+    launch), eager with host epochs and as a CUDA graph with device epochs."""
+    ins = wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    nbp = sar.sar_ll_packet_bytes(wl.count, wl.dtype)
+    pk = [torch.zeros(nbp, dtype=torch.uint8, device=dev) for _ in range(wl.nranks)]
+    res = torch.zeros(nbp, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ctrl = torch.zeros(2, dtype=torch.int32, device=dev)
+    pi, po, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in dout], [t.data_ptr() for t in pk]
+    epoch = [0]
+
+    def host_epoch_call():
+        epoch[0] += 1
+        sar.sar_allreduce_ll_writeback(pi, po, pp, res.data_ptr(), st.data_ptr(), multi_dest=multi_dest,
+                                       epoch=epoch[0], count=wl.count, dtype=wl.dtype, stream=stream.cuda_stream)
+
+    def device_epoch_call():
+        sar.sar_allreduce_ll_writeback(pi, po, pp, res.data_ptr(), st.data_ptr(), multi_dest=multi_dest,
+                                       epoch_ctrl=ctrl.data_ptr(), count=wl.count, dtype=wl.dtype,
+                                       stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_calls(torch, host_epoch_call, calls, stream)
+        ctrl[0] = epoch[0]
+        g_ms = time_graph(torch, device_epoch_call, calls, stream)
+    ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    mode = "multi_dest" if multi_dest else "own_output"
+    return {"workload": f"{wl.name}_writeback_{mode}", "calls": calls, "us_per_call": round(ms * 1e3, 3),
+            "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
+            "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
+            "status_ok": ok}
 
 
 def convert_row(torch, sar, dev, stream, count=1 << 26):
@@ -339,24 +421,60 @@ def run_gpu(args, d: Dist) -> None:
     with torch.cuda.stream(stream):
         g_ms = time_graph(torch, step, min(args.steps, 50), stream)
 
-    # End to end through the C ABI with host buffers: H2D of all inputs, the
-    # allreduce, D2H of all outputs, every step.
+    # End to end through the C ABI with host buffers: every step copies all
+    # inputs in from pinned host memory, runs the allreduce and copies all
+    # outputs back.  Pipelined in chunks over three streams (H2D, compute,
+    # D2H): chunk c's allreduce runs while chunk c+1 comes in and chunk c-1
+    # goes out; the next step's H2D of a chunk waits for this step's compute
+    # of it (the inputs are overwritten), and its compute waits for this
+    # step's D2H of it (the outputs are overwritten).
     h_in = [torch.from_numpy(x.view(NP_VIEW[wl.dtype])).pin_memory() for x in ins]
     h_out = [torch.empty(wl.count, dtype=din[0].dtype).pin_memory() for _ in range(wl.nranks)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    nchunk = 8
+    step_c = -(-wl.count // nchunk)
+    step_c = -(-step_c // 4096) * 4096
+    bounds = [(lo, min(wl.count, lo + step_c)) for lo in range(0, wl.count, step_c)]
+    es = din[0].element_size()
+    ev_in = [torch.cuda.Event() for _ in bounds]
+    ev_c = [torch.cuda.Event() for _ in bounds]
+    ev_out = [torch.cuda.Event() for _ in bounds]
+    first = [True]
 
     def e2e_step():
-        for h, t in zip(h_in, din):
-            t.copy_(h, non_blocking=True)
-        step()
-        for h, t in zip(h_out, dout):
-            h.copy_(t, non_blocking=True)
+        for c, (lo, hi) in enumerate(bounds):
+            if not first[0]:
+                s_in.wait_event(ev_c[c])
+            with torch.cuda.stream(s_in):
+                for h, t in zip(h_in, din):
+                    t[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                ev_in[c].record(s_in)
+            stream.wait_event(ev_in[c])
+            if not first[0]:
+                stream.wait_event(ev_out[c])
+            sar.sar_allreduce([p + lo * es for p in pi], [p + lo * es for p in po], count=hi - lo, dtype=wl.dtype,
+                              algo=sar.SAR_ALGO_RSAG, stream=stream.cuda_stream)
+            ev_c[c].record(stream)
+            s_out.wait_event(ev_c[c])
+            with torch.cuda.stream(s_out):
+                for h, t in zip(h_out, dout):
+                    h[lo:hi].copy_(t[lo:hi], non_blocking=True)
+                ev_out[c].record(s_out)
+        first[0] = False
 
-    e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_step()
+    torch.cuda.synchronize()
+    d.barrier()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(s_in)
+    for _ in range(e2e_steps):
         e2e_step()
-        d.barrier()
-        e2e_ms = d.max(time_calls(torch, e2e_step, e2e_steps, stream) * e2e_steps) / e2e_steps
-    e2e_ok = all(torch.equal(h_out[j], h_out[0]) for j in range(wl.nranks))
+    t_end.record(s_out)
+    t_end.synchronize()
+    e2e_ms = d.max(t_start.elapsed_time(t_end)) / e2e_steps
+    e2e_ok = all(torch.equal(h_out[j], h_out[0]) for j in range(wl.nranks)) and \
+        bool(torch.equal(h_out[0].to(dev), dout[0]))
     del h_in, h_out
 
     rows = []
@@ -367,14 +485,23 @@ def run_gpu(args, d: Dist) -> None:
         rows.append(rsag_row(torch, sar, W.C1, dev, stream, l2_bytes))
         for w in W.C3:
             rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes))
-        rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes))
+        c4_ins = W.C4.inputs()
+        rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins))
+        for acc in ("e4m3fn", "fp16"):
+            rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins, accum=acc))
+        rows.append(rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes))
         for w in W.C5:
             rows.append(ll_row(torch, sar, w, dev, stream, W.LL_CALLS))
+        for w in W.C5:
+            rows.append(ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS))
+        for w in W.C5:
+            for multi in (True, False):
+                rows.append(ll_writeback_row(torch, sar, w, dev, stream, W.LL_CALLS, multi))
         rows.append(convert_row(torch, sar, dev, stream))
 
     cpu = cpu_baseline(ins, wl) if d.rank == 0 and d.world == 1 and args.cpu_baseline else None
     sha = sources_sha()
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha"] == sha else None
+    traffic = TRAFFIC["bytes_per_launch"] if (TRAFFIC["sources_sha"] == sha and wl is W.C2) else None
     clk = clocks.summary(t0 - args.settle_s - 0.1, t1)
     if d.rank == 0:
         line = {
@@ -396,7 +523,10 @@ def run_gpu(args, d: Dist) -> None:
             "e2e": {"value": round(d.world * wl.algo_bytes / (e2e_ms * 1e-3) / GB, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": wl.nranks * wl.bytes_per_rank,
                     "d2h_bytes_per_step": wl.nranks * wl.bytes_per_rank, "steps": e2e_steps,
-                    "ms_per_step": round(e2e_ms, 3), "outputs_identical": e2e_ok},
+                    "ms_per_step": round(e2e_ms, 3), "outputs_identical": e2e_ok,
+                    "how": f"pinned host -> device copies, sar_allreduce, device -> pinned host copies of all "
+                           f"{wl.nranks} inputs and outputs every step, pipelined in {len(bounds)} chunks over "
+                           f"H2D / compute / D2H streams"},
             "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(kernel_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
@@ -438,7 +568,7 @@ def run_reference(args, d: Dist) -> None:
     print(json.dumps(line), flush=True)
 
 
-WORKLOADS = {w.name: w for w in [W.C1, W.C2, W.C4, W.C4_STRESS] + W.C3}
+WORKLOADS = {w.name: w for w in [W.C1, W.C2, W.C4, W.C4_STRESS, W.C4_B15] + W.C3}
 
 
 def main() -> None:

@@ -28,11 +28,14 @@
  *    into a CUDA graph.
  *  - `count` is the number of elements per rank.  count == 0 returns SAR_OK
  *    without launching anything.
- *  - Every argument error is returned before any launch.  Supported rank
- *    counts are 1, 2, 4, 8, 16 and 32; any other count returns
- *    SAR_ERR_UNSUPPORTED_NRANKS and launches nothing.  (In #948 the rsag
- *    kernel is instantiated only for 2, 4, 8, 16 and 32 ranks and other
- *    counts returned an error without launching.)
+ *  - Every argument error is returned before any launch.  nranks may be any
+ *    count from 1 to SAR_MAX_RANKS (32); other values return
+ *    SAR_ERR_UNSUPPORTED_NRANKS and launch nothing.  1, 2, 4, 8, 16 and 32
+ *    ranks run kernels with the rank loops unrolled at compile time (in #948
+ *    the rsag kernel exists only for 2, 4, 8, 16 and 32 ranks and other counts
+ *    returned an error without launching); every other count runs a kernel
+ *    that loops over the ranks at run time, in the same order, with the same
+ *    results.
  *  - Buffers must be aligned to their element size (else SAR_ERR_MISALIGNED).
  *    When every buffer of a call is 16-byte aligned the kernels move 16-byte
  *    vectors; otherwise a slower element-wise kernel runs.  Results are
@@ -67,8 +70,12 @@ typedef enum {
     SAR_BF16 = 0,        /* bfloat16, 2 bytes */
     SAR_FP16 = 1,        /* IEEE binary16, 2 bytes */
     SAR_FP32 = 2,        /* IEEE binary32, 4 bytes */
-    SAR_FP8_E4M3FN = 3   /* OCP FP8 E4M3 (bias 7, no inf, NaN = S.1111.111,
+    SAR_FP8_E4M3FN = 3,  /* OCP FP8 E4M3 (bias 7, no inf, NaN = S.1111.111,
                             max +-448; binary32 -> e4m3fn saturates), 1 byte */
+    SAR_FP8_E4M3B15 = 4  /* software FP8, bias 15, max finite 0.9375 (mscclpp
+                            commit history, "Add fp8_e4m3b15 datatype");
+                            S.1111.000 = inf, S.1111.mmm = NaN, binary32
+                            overflow rounds to inf, subnormals m/8 * 2^-14 */
 } sar_dtype;
 
 typedef enum {
@@ -79,7 +86,7 @@ typedef enum {
 typedef enum {
     SAR_OK = 0,
     SAR_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum, epoch 0, size overflow, ... */
-    SAR_ERR_UNSUPPORTED_NRANKS = 2, /* nranks not in {1, 2, 4, 8, 16, 32} */
+    SAR_ERR_UNSUPPORTED_NRANKS = 2, /* nranks outside 1..SAR_MAX_RANKS */
     SAR_ERR_UNSUPPORTED_DTYPE = 3,  /* dtype (or conversion pair) not supported */
     SAR_ERR_MISALIGNED = 4,         /* buffer not aligned to its element size (16 B for packets) */
     SAR_ERR_CUDA = 5,               /* a CUDA launch or copy failed */
@@ -110,6 +117,24 @@ typedef enum {
  */
 SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
                          sar_dtype dtype, sar_algo algo, sar_stream_t stream);
+
+/*
+ * sar_allreduce_accum -- the fused rsag allreduce with another accumulator
+ * (mscclpp commit history, "Add mixed-precision accumulation for allreduce":
+ * accumDtype, with AUTO resolving to the input type; FP8 inputs reduced in
+ * float16 or float32).
+ *
+ * Every partial sum is rounded into `accum`:
+ *   acc_0 = R_accum(f32(in[0][i])),
+ *   acc_k = R_accum(f32(acc_{k-1}) + f32(in[k][i]))   (binary32 add, then RNE),
+ *   out[j][i] = R_dtype(acc_{N-1}).
+ * accum: SAR_FP32 (identical to sar_allreduce with SAR_ALGO_RSAG), SAR_FP16,
+ * SAR_BF16, or `dtype` itself (native accumulation, e.g. e4m3fn with
+ * saturation at every step).  Other values return SAR_ERR_UNSUPPORTED_DTYPE.
+ * Buffers, chunking and errors as sar_allreduce.
+ */
+SAR_API sar_status sar_allreduce_accum(const void* const* in, void* const* out, int nranks, size_t count,
+                                       sar_dtype dtype, sar_dtype accum, sar_stream_t stream);
 
 /*
  * sar_reduce_scatter -- the rsag reduce step alone.
@@ -189,6 +214,58 @@ SAR_API sar_status sar_ll_unpack_reduce(const void* const* pkts, void* const* ou
 SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, void* const* pkts, int nranks,
                             size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
                             int32_t* d_status, sar_stream_t stream);
+
+/*
+ * sar_allreduce_ll_fused -- the LL all-pair allreduce in one cooperative
+ * launch: every block of simulated rank r packs its share of in[r] into
+ * pkts[r] (the send), then polls its share of rank r's packet chunk in all N
+ * packet buffers while other blocks are still packing, reduces in rank order
+ * and writes to all N outputs (mscclpp commit history, the
+ * allreduce_allpair_packet fix: send, reduce and write-back in the same
+ * thread block).  Results equal sar_allreduce_ll's.
+ *
+ * The launch is cooperative (all blocks co-resident), so blocks may wait on
+ * each other; a launch the device cannot make co-resident fails with
+ * SAR_ERR_CUDA.
+ *
+ * Epoch: with d_epoch == NULL the caller's `epoch` (non-zero, as in
+ * sar_ll_pack).  Otherwise d_epoch is a caller-owned device control block of
+ * two uint32 {last epoch, arrivals}, 8-byte aligned, zeroed once before first
+ * use: each launch uses last + 1 (skipping 0) and the last block to finish
+ * stores it, so a launch captured in a CUDA graph gets a fresh epoch on every
+ * replay; `epoch` is then ignored.  Packet buffers, max_spins and d_status as
+ * in sar_ll_unpack_reduce.  One control block must not be shared by launches
+ * that can overlap on the GPU.
+ */
+SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                                          size_t count, sar_dtype dtype, uint32_t epoch, uint32_t* d_epoch,
+                                          uint64_t max_spins, int32_t* d_status, sar_stream_t stream);
+
+/*
+ * sar_allreduce_ll_writeback -- the LL all-pair allreduce with the write-back
+ * as a second round of flagged packets, in one cooperative launch (mscclpp
+ * commit history: the allreduce_allpair_packet fix's send / reduce /
+ * write-back, and the ReadPutPacket change that reads packet data once and
+ * writes it to several destinations).
+ *
+ * As sar_allreduce_ll_fused, except that each rank's reduced chunk is written
+ * as packets (flag = epoch) into the result packet buffer `res` and then
+ * polled again and unpacked into the outputs:
+ *   multi_dest != 0 : each result packet is read once and written to all N
+ *                     outputs (by the blocks of another rank than its reducer);
+ *   multi_dest == 0 : every rank reads every result packet and writes its own
+ *                     output (N reads per packet).
+ * Results equal sar_allreduce_ll's; after the call `res` holds the packets of
+ * the reduced data, zero-padded like sar_ll_pack's.
+ *
+ * res : caller-owned device buffer of sar_ll_packet_bytes(count, dtype) bytes,
+ *       16-byte aligned, zeroed once before first use; the same epoch rules as
+ *       the send packet buffers.
+ */
+SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const* out, void* const* pkts, void* res,
+                                              int nranks, size_t count, sar_dtype dtype, uint32_t epoch,
+                                              uint32_t* d_epoch, int multi_dest, uint64_t max_spins,
+                                              int32_t* d_status, sar_stream_t stream);
 
 /*
  * Size of the fixed LL packet scratch inside the library used by

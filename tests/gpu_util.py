@@ -8,8 +8,8 @@ import torch
 GUARD = 256          # bytes of canary before and after every buffer
 CANARY = 0xA5
 
-STORE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8}
-ESIZE = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3fn": 1}
+STORE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8, "e4m3b15": np.uint8}
+ESIZE = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3fn": 1, "e4m3b15": 1}
 
 
 class Guarded:
@@ -55,6 +55,8 @@ def is_nan_code(codes: np.ndarray, dt: str) -> np.ndarray:
         c = c.view(np.uint16)
         return ((c & 0x7C00) == 0x7C00) & ((c & 0x03FF) != 0)
     c = c.view(np.uint8)
+    if dt == "e4m3b15":
+        return ((c & 0x78) == 0x78) & ((c & 0x07) != 0)
     return (c & 0x7F) == 0x7F
 
 

@@ -59,7 +59,7 @@ def test_status_strings(sar):
     assert "unknown" in sar.sar_status_string(99)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn"])
+@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn", "e4m3b15"])
 def test_chunk_rule_matches_oracle(sar, dt):
     for count in (0, 1, 7, 9, 4097, 1 << 20, (1 << 25) + 3):
         for n in (1, 2, 4, 8, 16, 32):
@@ -68,10 +68,13 @@ def test_chunk_rule_matches_oracle(sar, dt):
             if n > 1 and b < count:
                 assert b == c
             assert all(oracle.rsag_chunk(count, n, dt, r)[0] == min(count, r * c) for r in range(n))
-    assert sar.sar_rsag_chunk(10, 3, dt) == 0
+    assert sar.sar_rsag_chunk(10, 33, dt) == 0 and sar.sar_rsag_chunk(10, 0, dt) == 0
+    for n in (3, 5, 6, 7, 12, 31):                      # any count up to 32 is valid
+        c = sar.sar_rsag_chunk(100003, n, dt)
+        assert c == oracle.rsag_chunk(100003, n, dt, 1)[0]
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn"])
+@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn", "e4m3b15"])
 def test_packet_bytes_match_oracle(sar, dt):
     for count in (0, 1, 2, 3, 5, 1000, 262144):
         assert sar.sar_ll_packet_bytes(count, dt) == 8 * oracle.ll_packets(count, dt)
@@ -85,11 +88,11 @@ def _arr(vals):
 def test_argument_errors_before_launch(sar):
     L = sar.lib
     ptrs2 = _arr([4096, 8192])
-    # unsupported rank counts (the #948 set plus 1)
-    for n in (0, 3, 5, 6, 7, 9, 33, -1):
+    # rank counts outside 1..32
+    for n in (0, 33, 64, -1):
         assert L.sar_allreduce(ptrs2, ptrs2, n, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
         assert L.sar_ll_pack(ptrs2, ptrs2, n, 16, sar.SAR_BF16, 1, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
-    assert L.sar_allreduce(ptrs2, ptrs2, 2, 16, 4, 0, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_allreduce(ptrs2, ptrs2, 2, 16, 5, 0, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_allreduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 7, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_allreduce(None, ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_allreduce(_arr([4096, 0]), ptrs2, 2, 16, sar.SAR_BF16, 0, None) == sar.SAR_ERR_INVALID_ARG
@@ -106,10 +109,12 @@ def test_argument_errors_before_launch(sar):
     assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 100, None, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 0, 4096, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_ll_unpack_reduce(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4098, None) == sar.SAR_ERR_MISALIGNED
-    assert L.sar_allreduce_ll(ptrs2, ptrs2, ptrs2, 3, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
+    assert L.sar_allreduce_ll(ptrs2, ptrs2, ptrs2, 33, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
         sar.SAR_ERR_UNSUPPORTED_NRANKS
     assert L.sar_allreduce_ll(ptrs2, None, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4096, None) == sar.SAR_ERR_INVALID_ARG
-    # conversion pairs
+    # conversion pairs: one side FP8 (e4m3fn or e4m3b15), the other fp32/fp16/bf16
+    assert L.sar_fp8_convert(4096, sar.SAR_FP8_E4M3FN, 8192, sar.SAR_FP8_E4M3B15, 16, None) == \
+        sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_fp8_convert(4096, sar.SAR_FP32, 8192, sar.SAR_BF16, 16, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_fp8_convert(4096, sar.SAR_FP8_E4M3FN, 8192, sar.SAR_FP8_E4M3FN, 16, None) == \
         sar.SAR_ERR_UNSUPPORTED_DTYPE
@@ -117,9 +122,31 @@ def test_argument_errors_before_launch(sar):
     assert L.sar_fp8_convert(None, sar.SAR_FP32, 8192, sar.SAR_FP8_E4M3FN, 16, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_fp8_convert(4096, sar.SAR_FP32, 8192, sar.SAR_FP8_E4M3FN, 0, None) == sar.SAR_OK
     assert L.sar_read_device_status(None, None) == sar.SAR_ERR_INVALID_ARG
+    # accumulation types: fp32, fp16, bf16 or the input type itself
+    assert L.sar_allreduce_accum(ptrs2, ptrs2, 0, 16, sar.SAR_BF16, sar.SAR_FP16, None) == \
+        sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce_accum(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, sar.SAR_FP8_E4M3FN, None) == \
+        sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_allreduce_accum(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 9, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
+    assert L.sar_allreduce_accum(ptrs2, ptrs2, 2, 0, sar.SAR_FP8_E4M3FN, sar.SAR_FP8_E4M3FN, None) == sar.SAR_OK
+    # fused LL: host epoch 0 is reserved unless a device control block supplies it
+    assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_FP32, 0, None, 9, 4096, None) == \
+        sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_FP32, 0, 4100, 9, 4096, None) == \
+        sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 2, 0, sar.SAR_FP32, 0, 4096, 9, 4096, None) == sar.SAR_OK
+    assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 40, 16, sar.SAR_FP32, 1, None, 9, 4096, None) == \
+        sar.SAR_ERR_UNSUPPORTED_NRANKS
+    # packet write-back: result buffer required and 16-byte aligned
+    assert L.sar_allreduce_ll_writeback(ptrs2, ptrs2, ptrs2, None, 2, 16, sar.SAR_FP32, 1, None, 1, 9, 4096,
+                                        None) == sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce_ll_writeback(ptrs2, ptrs2, ptrs2, 4104, 2, 16, sar.SAR_FP32, 1, None, 1, 9, 4096,
+                                        None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce_ll_writeback(ptrs2, ptrs2, ptrs2, 4096, 2, 16, sar.SAR_FP32, 0, None, 1, 9, 4096,
+                                        None) == sar.SAR_ERR_INVALID_ARG
 
 
 def test_binding_raises_on_error(sar):
     with pytest.raises(sar.SarError) as ei:
-        sar.sar_allreduce([4096] * 3, [8192] * 3, count=16, dtype="bf16", stream=0)
+        sar.sar_allreduce([4096] * 33, [8192] * 33, count=16, dtype="bf16", stream=0)
     assert ei.value.status == sar.SAR_ERR_UNSUPPORTED_NRANKS

@@ -29,21 +29,33 @@ def _convert(sar, src_codes, src, dst, offset=0):
     return g_dst.codes(dst)
 
 
+@pytest.mark.parametrize("fp8", ["e4m3fn", "e4m3b15"])
 @pytest.mark.parametrize("offset", [0, 1])
 @pytest.mark.parametrize("dst", ["fp32", "fp16", "bf16"])
-def test_every_e4m3fn_code_widens_exactly(sar, dst, offset):
+def test_every_fp8_code_widens_exactly(sar, dst, offset, fp8):
     codes = np.tile(np.arange(256, dtype=np.uint8), 9)[:2300]      # groups of 16 plus a tail
-    got = _convert(sar, codes, "e4m3fn", dst, offset)
-    assert_same(got, oracle.convert(codes, "e4m3fn", dst), dst)
+    got = _convert(sar, codes, fp8, dst, offset)
+    assert_same(got, oracle.convert(codes, fp8, dst), dst)
 
 
+@pytest.mark.parametrize("fp8", ["e4m3fn", "e4m3b15"])
 @pytest.mark.parametrize("offset", [0, 3])
 @pytest.mark.parametrize("src", ["fp16", "bf16"])
-def test_every_16bit_code_narrows_once(sar, src, offset):
+def test_every_16bit_code_narrows_once(sar, src, offset, fp8):
     codes = np.arange(1 << 16, dtype=np.uint16)
     codes = np.concatenate([codes, codes[:7]])
-    got = _convert(sar, codes, src, "e4m3fn", offset)
-    assert_same(got, oracle.convert(codes, src, "e4m3fn"), "e4m3fn")
+    got = _convert(sar, codes, src, fp8, offset)
+    assert_same(got, oracle.convert(codes, src, fp8), fp8)
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_binary32_rounding_cases_narrow_once_e4m3b15(sar, offset):
+    x = _f32_points()
+    x = np.concatenate([x, np.array([np.inf, -np.inf, np.nan, 0.9375, 0.96875, 0.968, 1.0, -1e30], np.float32)])
+    got = _convert(sar, x, "fp32", "e4m3b15", offset)
+    assert_same(got, oracle.convert(x, "fp32", "e4m3b15"), "e4m3b15")
+    assert got[-8:].tolist() == [0x78, 0xF8, got[-6], 0x77, 0x78, 0x77, 0x78, 0xF8]
+    assert got[-6] & 0x78 == 0x78 and got[-6] & 0x07 != 0        # NaN stays NaN
 
 
 @pytest.mark.parametrize("offset", [0, 1])

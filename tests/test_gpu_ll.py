@@ -12,7 +12,7 @@ from tests.gpu_util import ESIZE, Guarded, assert_same, random_codes
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ["bf16", "fp16", "fp32", "e4m3fn"]
+DTYPES = ["bf16", "fp16", "fp32", "e4m3fn", "e4m3b15"]
 
 
 @pytest.fixture(scope="module")
@@ -30,7 +30,7 @@ def _packets(sar, n, count, dt, fill=0):
 
 
 @pytest.mark.parametrize("count", [1, 2, 3, 5, 8, 33, 1031, 65541])
-@pytest.mark.parametrize("n", [1, 2, 8, 32])
+@pytest.mark.parametrize("n", [1, 2, 3, 6, 8, 32])
 @pytest.mark.parametrize("dt", DTYPES)
 def test_pack_unpack_match_oracle(sar, dt, n, count):
     rng = np.random.default_rng([DTYPES.index(dt), n, count])

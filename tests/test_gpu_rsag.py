@@ -14,8 +14,9 @@ from tests.gpu_util import ESIZE, Guarded, assert_same, random_codes
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ["bf16", "fp16", "fp32", "e4m3fn"]
+DTYPES = ["bf16", "fp16", "fp32", "e4m3fn", "e4m3b15"]
 RANKS = [1, 2, 4, 8, 16, 32]
+ODD_RANKS = [3, 5, 6, 7, 12, 31]          # counts with a runtime rank loop
 
 
 @pytest.fixture(scope="module")
@@ -57,11 +58,37 @@ def test_allreduce_matches_oracle(sar, dt, n, count, algo):
 
 
 @pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("count", [1, 9, 4097, 100003])
+@pytest.mark.parametrize("n", ODD_RANKS)
+@pytest.mark.parametrize("dt", DTYPES)
+def test_any_rank_count(sar, dt, n, count, algo):
+    """Rank counts outside {1, 2, 4, 8, 16, 32} (rejected by the rsag kernel of
+    #948) run a kernel with a runtime rank loop; same order, same bits."""
+    rng = np.random.default_rng([DTYPES.index(dt), n, count, algo, 1])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, algo)
+    _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("n", [3, 7])
+def test_any_rank_count_unaligned_and_in_place(sar, n):
+    rng = np.random.default_rng(n)
+    ins = [random_codes(rng, "bf16", 3001) for _ in range(n)]
+    want = oracle.allreduce(ins, "bf16")[0]
+    gin, gout = _run(sar, ins, "bf16", 0, offsets=[2 * (r % 3) for r in range(n)])
+    _check(gin, gout, ins, want, "bf16")
+    gin, gout = _run(sar, ins, "bf16", 1, inplace=True)
+    _check(gin, gout, ins, want, "bf16", inplace=True)
+
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
 @pytest.mark.parametrize("dt", DTYPES)
 def test_many_tiles_and_ragged_tail(sar, dt, algo):
     """Several tiles per rank chunk plus a partial last vector."""
     count = (1 << 21) + 13
-    ins = W.rank_inputs("normal", 5, dt, count, 8, 4.0 if dt == "e4m3fn" else 1.0)
+    sigma = {"e4m3fn": 4.0, "e4m3b15": 0.1}.get(dt, 1.0)
+    ins = W.rank_inputs("normal", 5, dt, count, 8, sigma)
     want = oracle.allreduce(ins, dt)[0]
     gin, gout = _run(sar, ins, dt, algo)
     _check(gin, gout, ins, want, dt)
@@ -109,7 +136,7 @@ def test_rank_order_is_fixed(sar):
             assert np.all(g.codes("fp32") == 1.0)
 
 
-NEG_ZERO = {"bf16": 0x8000, "fp16": 0x8000, "e4m3fn": 0x80}
+NEG_ZERO = {"bf16": 0x8000, "fp16": 0x8000, "e4m3fn": 0x80, "e4m3b15": 0x80}
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -126,7 +153,7 @@ def test_single_rank_is_identity_including_negative_zero(sar, dt):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
-@pytest.mark.parametrize("n", [2, 4, 8, 32])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 13, 32])
 def test_reduce_scatter_then_all_gather(sar, dt, n):
     rng = np.random.default_rng(n + 7)
     count = 20011
@@ -166,8 +193,8 @@ def test_graph_capture_and_replay(sar):
     with torch.cuda.graph(graph, stream=s):
         sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout], count=count, dtype=dt, algo=0)
         sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout2], count=count, dtype=dt, algo=1)
-        with pytest.raises(sar.SarError):       # rejected before launch, capture unaffected
-            sar.sar_allreduce([g.ptr for g in gin[:3]], [g.ptr for g in gout[:3]], count=count, dtype=dt)
+        with pytest.raises(sar.SarError):       # bad dtype: rejected before launch, capture unaffected
+            sar.sar_allreduce([g.ptr for g in gin[:3]], [g.ptr for g in gout[:3]], count=count, dtype=9)
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()

@@ -69,7 +69,7 @@ def test_noalloc_rejects_sizes_beyond_the_array(sar):
     rc = L.sar_allreduce_ll_noalloc(_ptrs(bufs), _ptrs(bufs), n, too_big, sar.DTYPE_CODES[dt], 1 << 20, None,
                                     torch.cuda.current_stream().cuda_stream)
     assert rc == sar.SAR_ERR_INVALID_ARG
-    rc = L.sar_allreduce_ll_noalloc(_ptrs(bufs), _ptrs(bufs), 3, 16, sar.DTYPE_CODES[dt], 1 << 20, None, None)
+    rc = L.sar_allreduce_ll_noalloc(_ptrs(bufs), _ptrs(bufs), 33, 16, sar.DTYPE_CODES[dt], 1 << 20, None, None)
     assert rc == sar.SAR_ERR_UNSUPPORTED_NRANKS
     rc = L.sar_allreduce_ll_noalloc(_ptrs(bufs), _ptrs(bufs), n, 16, sar.DTYPE_CODES[dt], 0, None, None)
     assert rc == sar.SAR_ERR_INVALID_ARG

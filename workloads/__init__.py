@@ -23,7 +23,9 @@ Distributions:
 Quantisation to the element type goes through library conversions, all
 round-to-nearest-even from binary32: numpy for binary16, torch for bfloat16
 and float8_e4m3fn (after clamping to +-448, which makes torch's
-non-saturating conversion saturate).
+non-saturating conversion saturate).  e4m3b15 has no library conversion: its
+values are rounded to binary16 by numpy and then to 3 fraction bits (a double
+rounding, which only decides which input values are drawn).
 """
 from __future__ import annotations
 
@@ -37,8 +39,8 @@ _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-ESIZE = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3fn": 1}
-STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8}
+ESIZE = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3fn": 1, "e4m3b15": 1}
+STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "e4m3fn": np.uint8, "e4m3b15": np.uint8}
 
 
 def splitmix64(seed: int, k: np.ndarray) -> np.ndarray:
@@ -79,6 +81,17 @@ def quantise(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "e4m3fn":
         t = t.clamp(-448.0, 448.0)
         return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    if dtype == "e4m3b15":
+        # Same bias as binary16, so a finite e4m3b15 code is the top byte of a
+        # binary16 with 3 fraction bits: round to binary16 (numpy RNE), then
+        # round the 7 dropped fraction bits to nearest even (a double
+        # rounding; it only picks the input values).  Values are clamped to
+        # +-0.9375 first.
+        h = np.clip(x, -0.9375, 0.9375).astype(np.float16).view(np.uint16).astype(np.uint32)
+        mag = h & 0x7FFF
+        keep, rest = mag >> 7, mag & 0x7F
+        keep = keep + ((rest > 0x40) | ((rest == 0x40) & (keep & 1) == 1)).astype(np.uint32)
+        return (((h >> 8) & 0x80) | keep).astype(np.uint8)
     raise ValueError(f"unknown dtype {dtype}")
 
 
@@ -171,6 +184,9 @@ C3 = [Workload(f"rsag_2x{(8192 << (2 * k)) * 2 // KiB}KiB_bf16", 2, "bf16", 8192
 C4 = Workload("rsag_8x16MiB_e4m3fn", 8, "e4m3fn", 16 * MiB, "normal", 2, 4.0)
 # Added stress set for the saturation edge (sigma 256).
 C4_STRESS = Workload("rsag_8x16MiB_e4m3fn_sigma256", 8, "e4m3fn", 16 * MiB, "normal", 2, 256.0)
+# Added counterpart of the e4m3fn workload for the software e4m3b15 type
+# (max finite 0.9375): 8 ranks, 16M elements, N(0, 0.05^2).
+C4_B15 = Workload("rsag_8x16MiB_e4m3b15", 8, "e4m3b15", 16 * MiB, "normal", 2, 0.05)
 # 8 ranks, LL all-pair, fp32 and bf16, 1 KiB .. 1 MiB per rank in x4 steps, uniform, seed 3.
 C5 = [Workload(f"ll_8x{s // KiB}KiB_{dt}", 8, dt, s // ESIZE[dt], "uniform", 3, algo="ll")
       for dt in ("fp32", "bf16") for s in (1 * KiB, 4 * KiB, 16 * KiB, 64 * KiB, 256 * KiB, 1 * MiB)]
