@@ -1,14 +1,15 @@
-// convert.cu -- e4m3fn <-> {fp32, fp16, bf16}.
+// convert.cu -- FP8 (e4m3fn, e4m3b15) <-> {fp32, fp16, bf16}.
 //
-// mscclpp commit history (the ROCm FP8 summary and "Add mixed-precision
-// accumulation for allreduce"): FP8 data is reduced in a wider type, which
-// needs the exact widening e4m3fn -> binary32 and the single saturating
-// rounding binary32 -> e4m3fn used inside the reduction kernels.  This entry
-// point exposes the same two conversions on their own: dst = R_dst(f32(src)).
-// Widening from e4m3fn is exact into every wider type; narrowing rounds once
-// to nearest-even with satfinite (finite overflow and infinities -> +-448,
-// NaN -> NaN).  Each lane converts 4 consecutive elements per access, so a
-// warp's loads and stores each cover one contiguous run of memory.
+// mscclpp commit history (the ROCm FP8 summary, "Add fp8_e4m3b15 datatype"
+// and "Add mixed-precision accumulation for allreduce"): FP8 data is reduced
+// in a wider type, which needs the exact widening FP8 -> binary32 and the
+// single rounding binary32 -> FP8 used inside the reduction kernels.  This
+// entry point exposes the same conversions on their own: dst = R_dst(f32(src)).
+// Widening is exact into every wider type; narrowing rounds once to
+// nearest-even (e4m3fn: satfinite, finite overflow and infinities -> +-448;
+// e4m3b15: overflow -> infinity; NaN -> NaN).  Each lane converts 4
+// consecutive elements per access, so a warp's loads and stores each cover
+// one contiguous run of memory.
 #include "sar_device.cuh"
 #include "sar_internal.h"
 

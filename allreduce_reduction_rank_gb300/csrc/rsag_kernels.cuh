@@ -41,6 +41,13 @@ template <> struct Shape<0> {
     static constexpr int kUnroll = 2;
 };
 
+// Vectors per thread: the FP8 types carry 16 elements per vector and spend
+// more registers and instructions on widening, so one vector per thread keeps
+// more warps resident (measured: e4m3b15 +18%, e4m3fn +2% on 8 x 16 MiB).
+template <int DT, int NR> struct UnrollOf {
+    static constexpr int k = (DT == SAR_FP8_E4M3FN || DT == SAR_FP8_E4M3B15) ? 1 : Shape<NR>::kUnroll;
+};
+
 // x -> R_acc(x) as a binary32 value.
 template <int ACC> __device__ __forceinline__ float round_acc(float x);
 template <> __device__ __forceinline__ float round_acc<SAR_FP32>(float x) { return x; }
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(kThreads)
 vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
     constexpr int VE = Elem<DT>::kVE;
     constexpr int WIN = Shape<NR>::kWin;
-    constexpr int UNROLL = Shape<NR>::kUnroll;
+    constexpr int UNROLL = UnrollOf<DT, NR>::k;
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
     if (begin >= count) return;
@@ -206,7 +213,7 @@ constexpr size_t kScalarGridX = 8192;
 template <int DT, int NR, int MODE, int ACC>
 cudaError_t launch_vec(const RankPtrs& p, int nranks, size_t count, size_t chunk, cudaStream_t s) {
     constexpr int VE = Elem<DT>::kVE;
-    const size_t tile = static_cast<size_t>(kThreads) * Shape<NR>::kUnroll;
+    const size_t tile = static_cast<size_t>(kThreads) * UnrollOf<DT, NR>::k;
     const dim3 grid(grid_x((chunk + VE - 1) / VE, tile, kMaxGridX), nranks);
     vec_kernel<DT, NR, MODE, ACC><<<grid, kThreads, 0, s>>>(p, nranks, count, chunk);
     return cudaGetLastError();

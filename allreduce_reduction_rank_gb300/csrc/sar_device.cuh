@@ -6,8 +6,9 @@
 // element is widened exactly to binary32, the ranks are added in order
 // 0..N-1 with IEEE round-to-nearest-even adds (__fadd_rn: never contracted,
 // never flushed; this library is built without fast-math or ftz), and the sum
-// is rounded once to the element type with the hardware cvt.rn conversions
-// (satfinite for e4m3fn).
+// is rounded once to the element type: the hardware cvt.rn conversions for
+// bf16, fp16 and e4m3fn (satfinite), software round-to-nearest-even for the
+// e4m3b15 type, which has no hardware conversion.
 #pragma once
 
 #include <cstddef>
@@ -69,7 +70,7 @@ __device__ __forceinline__ uint32_t f32_to_e4m3b15(float x) {
 }
 
 // Exact widening of one 32-bit word holding 2 (16-bit types), 1 (fp32) or
-// 4 (e4m3fn) elements, lowest address first.
+// 4 (FP8 types) elements, lowest address first.
 template <int DT> __device__ __forceinline__ void widen_word(uint32_t w, float* x);
 
 template <> __device__ __forceinline__ void widen_word<SAR_BF16>(uint32_t w, float* x) {
