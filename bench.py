@@ -43,11 +43,11 @@ GB = 1e9
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic of one launch of the dominant kernel (rsag fused, fp16, 8 ranks,
-# 64 MiB per rank) from one ncu capture (dram__bytes_read.sum 536,978,432 +
-# dram__bytes_write.sum 487,227,648; the rest of the 536.9 MB of outputs is
+# 64 MiB per rank) from one ncu capture (dram__bytes_read.sum 536,983,808 +
+# dram__bytes_write.sum 487,242,496; the rest of the 536.9 MB of outputs is
 # still dirty in L2 when the launch ends), valid while the kernel sources hash
 # to `sources_sha`; otherwise `traffic` is reported as null.
-TRAFFIC = {"sources_sha": "48e7ed87f073df85", "bytes_per_launch": 1024206080}
+TRAFFIC = {"sources_sha": "a4a11314b64d9c4a", "bytes_per_launch": 1024226304}
 KERNEL_SOURCES = ["allreduce_reduction_rank_gb300/csrc/rsag_kernels.cuh",
                   "allreduce_reduction_rank_gb300/csrc/rsag_fp16.cu",
                   "allreduce_reduction_rank_gb300/csrc/sar_device.cuh"]
@@ -188,12 +188,13 @@ def time_graph(torch, fn, calls: int, stream) -> float:
     with torch.cuda.graph(graph, stream=stream):
         for _ in range(calls):
             fn()
-    graph.replay()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    graph.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):        # replay() launches on the current stream
+        graph.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
     end.synchronize()
     return start.elapsed_time(end) / calls
 
@@ -472,9 +473,89 @@ def run_gpu(args, d: Dist) -> None:
         e2e_step()
     t_end.record(s_out)
     t_end.synchronize()
-    e2e_ms = d.max(t_start.elapsed_time(t_end)) / e2e_steps
+    eager_ms = d.max(t_start.elapsed_time(t_end)) / e2e_steps
     e2e_ok = all(torch.equal(h_out[j], h_out[0]) for j in range(wl.nranks)) and \
         bool(torch.equal(h_out[0].to(dev), dout[0]))
+
+    # The same pipelined steps captured in a CUDA graph (4 steps per graph, so
+    # consecutive steps still overlap inside it): no host launch overhead.
+    per_graph = 4
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        first[0] = True
+        for _ in range(per_graph):
+            e2e_step()
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+    for h in h_out:
+        h.zero_()
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    graph_ok = all(torch.equal(h_out[j].to(dev), dout[0]) for j in range(wl.nranks))
+    replays = max(1, e2e_steps // per_graph)
+    with torch.cuda.stream(stream):          # replay() launches on the current stream
+        t_start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        t_end.record(stream)
+    t_end.synchronize()
+    graph_ms = d.max(t_start.elapsed_time(t_end)) / (replays * per_graph)
+    del graph
+
+    # Zero copy: the kernel reads the pinned host inputs and writes the pinned
+    # host outputs itself over the CPU-GPU link (one launch per step).
+    hi_p, ho_p = [h.data_ptr() for h in h_in], [h.data_ptr() for h in h_out]
+
+    def zero_copy_step():
+        sar.sar_allreduce(hi_p, ho_p, count=wl.count, dtype=wl.dtype, algo=sar.SAR_ALGO_RSAG,
+                          stream=stream.cuda_stream)
+
+    for h in h_out:
+        h.zero_()
+    with torch.cuda.stream(stream):
+        zero_copy_step()
+        torch.cuda.synchronize()
+        zc_ok = all(torch.equal(h_out[j].to(dev), dout[0]) for j in range(wl.nranks))
+        zc_ms = d.max(time_calls(torch, zero_copy_step, max(3, e2e_steps // 2), stream))
+    e2e_ms = min(eager_ms, graph_ms)
+    e2e_ok = e2e_ok and graph_ok
+
+    # The platform's ceiling for that traffic: the same pinned copies alone
+    # (H2D of all inputs, D2H of all outputs) and both directions at once.
+    def copy_ms(direction: str, reps: int = 5) -> float:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        s_out.wait_event(t0)
+        for _ in range(reps):
+            if direction in ("h2d", "both"):
+                with torch.cuda.stream(s_in):
+                    for h, t in zip(h_in, din):
+                        t.copy_(h, non_blocking=True)
+            if direction in ("d2h", "both"):
+                with torch.cuda.stream(s_out):
+                    for h, t in zip(h_out, dout):
+                        h.copy_(t, non_blocking=True)
+        s_in.wait_stream(s_out)
+        t1.record(s_in)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    io_bytes = wl.nranks * wl.bytes_per_rank
+    h2d_ms, d2h_ms, both_ms = copy_ms("h2d"), copy_ms("d2h"), copy_ms("both")
+    # A step moves io_bytes each way; it cannot beat the copies alone by more
+    # than timing noise, so a faster figure means the timing is wrong.
+    if e2e_ms < 0.9 * both_ms:
+        raise RuntimeError(f"e2e step {e2e_ms:.3f} ms beats its own copies ({both_ms:.3f} ms): timing error")
+    copy_limits = {"h2d_GBps": round(io_bytes / (h2d_ms * 1e-3) / GB, 1),
+                   "d2h_GBps": round(io_bytes / (d2h_ms * 1e-3) / GB, 1),
+                   "both_directions_GBps": round(2 * io_bytes / (both_ms * 1e-3) / GB, 1),
+                   "both_directions_ms_per_step": round(both_ms, 3),
+                   "e2e_vs_copies_alone": round(both_ms / e2e_ms, 3)}
     del h_in, h_out
 
     rows = []
@@ -526,7 +607,15 @@ def run_gpu(args, d: Dist) -> None:
                     "ms_per_step": round(e2e_ms, 3), "outputs_identical": e2e_ok,
                     "how": f"pinned host -> device copies, sar_allreduce, device -> pinned host copies of all "
                            f"{wl.nranks} inputs and outputs every step, pipelined in {len(bounds)} chunks over "
-                           f"H2D / compute / D2H streams"},
+                           f"H2D / compute / D2H streams (faster of eager and CUDA-graph issue)",
+                    "copy_limits": copy_limits,
+                    "variants_ms_per_step": {"pipelined_eager": round(eager_ms, 3),
+                                             "pipelined_cuda_graph": round(graph_ms, 3),
+                                             "zero_copy_kernel": round(zc_ms, 3)},
+                    "zero_copy": {"value": round(d.world * wl.algo_bytes / (zc_ms * 1e-3) / GB, 2),
+                                  "outputs_ok": zc_ok,
+                                  "how": "sar_allreduce on the pinned host buffers themselves: the kernel's "
+                                         "loads and stores cross the CPU-GPU link, no copies"}},
             "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(kernel_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
@@ -540,12 +629,21 @@ def run_gpu(args, d: Dist) -> None:
 
 
 def run_reference(args, d: Dist) -> None:
-    """The CPU oracle as it stands, on a bounded sample of the same workload."""
+    """The CPU oracle as it stands, on a bounded sample of the same workload:
+    the first `sample` elements of each rank, with `sample` chosen so that the
+    whole --warmup + --steps run takes about a minute of CPU time."""
     if d.rank != 0:
         return
     import oracle
     wl = W.C2
-    sample = 1 << 19
+    probe = 1 << 14
+    ins = [W.rank_input(wl.dist, wl.seed, wl.dtype, probe, r, wl.sigma) for r in range(wl.nranks)]
+    t = time.perf_counter()
+    oracle.allreduce(ins, wl.dtype)
+    per_elem = max(1e-9, (time.perf_counter() - t) / probe)
+    budget_s = 60.0
+    sample = int(budget_s / ((args.steps + args.warmup) * per_elem))
+    sample = max(probe, min(1 << 20, sample)) // 256 * 256
     ins = [W.rank_input(wl.dist, wl.seed, wl.dtype, sample, r, wl.sigma) for r in range(wl.nranks)]
     for _ in range(args.warmup):
         oracle.allreduce(ins, wl.dtype)
@@ -555,15 +653,14 @@ def run_reference(args, d: Dist) -> None:
     el = time.perf_counter() - t
     bytes_ = 2 * wl.nranks * sample * W.ESIZE[wl.dtype]
     value = bytes_ * args.steps / el / GB
+    what = f"first {sample} elements of each of the {wl.nranks} ranks of {wl.name} per step"
     line = {"impl": "reference", "metric": "simulated-allreduce HBM GB/s (% of GB300 peak) and us/call vs message size",
             "value": round(value, 4), "unit": "GB/s", "n_gpus": d.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": wl.name, "nranks": wl.nranks, "count_per_rank": wl.count,
-                       "algo": "rsag (oracle: plain rank-ordered sum)",
-                       "sample": f"first {sample} elements of each rank per step"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"first {sample} elements of each of the {wl.nranks} ranks per step"},
+                       "algo": "rsag (oracle: plain rank-ordered sum)", "sample": what},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

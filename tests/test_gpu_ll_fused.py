@@ -125,3 +125,23 @@ def test_thousand_fused_calls(sar, wl):
             for g in gout:
                 assert_same(g.codes(dt), want, dt, f"epoch {epoch}")
     assert sar.sar_read_device_status(st) == sar.SAR_OK
+
+
+def test_device_epoch_wraps_past_zero(sar):
+    """The device counter at 2^32 - 1: the next epoch skips the reserved 0."""
+    n, count, dt = 4, 3001, "fp32"
+    rng = np.random.default_rng(12)
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin = [Guarded.from_codes(c) for c in ins]
+    gout = [Guarded(count * 4) for _ in range(n)]
+    pk = _packets(sar, n, count, dt)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctrl = torch.tensor([-1, 0], dtype=torch.int32, device="cuda")      # last epoch 0xFFFFFFFF
+    sar.sar_allreduce_ll_fused([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], st,
+                               epoch_ctrl=ctrl, count=count, dtype=dt)
+    assert sar.sar_read_device_status(st) == sar.SAR_OK
+    assert ctrl.cpu().tolist() == [1, 0]
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+    assert np.array_equal(pk[0].bytes(), oracle.ll_pack(ins, dt, 1)[0])
