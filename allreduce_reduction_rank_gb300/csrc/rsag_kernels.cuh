@@ -66,20 +66,103 @@ template <> __device__ __forceinline__ float round_acc<SAR_FP8_E4M3B15>(float x)
     return e4m3b15_to_f32(f32_to_e4m3b15(x));
 }
 
-template <int DT, int ACC> __device__ __forceinline__ void seed(Acc<DT>& a, const uint4& v) {
-    acc_seed<DT>(a, v);
-    if constexpr (ACC != SAR_FP32) {
+// e4m3b15 with the binary32 accumulator sums 2^8 times the values on the
+// e4m3fn conversions (exact, see e4m3b15_widen_scaled); every other vector
+// case widens to the values themselves.
+template <int DT, int ACC> struct ScaledB15 {
+    static constexpr bool k = DT == SAR_FP8_E4M3B15 && ACC == SAR_FP32;
+};
+
+// e4m3fn accumulated in e4m3fn ("native") keeps its 16 partial sums as e4m3fn
+// values in 8 f16x2 words; a step is one f16x2 add and a round trip through
+// the saturating e4m3fn conversion.  This is R(acc + x) exactly: the binary32
+// add of two e4m3fn values is exact (multiples of 2^-9 below 2^10), and for
+// every one of the 65536 pairs of e4m3fn codes the e4m3fn rounding of their
+// binary16 sum equals the e4m3fn rounding of their exact sum (checked
+// exhaustively; the binary16 sum is inexact only where the difference cannot
+// reach an e4m3fn rounding boundary).
+struct AccFn8 { uint32_t h[8]; };
+
+template <int DT, int ACC> struct NativeFn8 {
+    static constexpr bool k = DT == SAR_FP8_E4M3FN && ACC == SAR_FP8_E4M3FN;
+};
+
+template <int DT, int ACC> struct AccOf { using T = Acc<DT>; };
+template <> struct AccOf<SAR_FP8_E4M3FN, SAR_FP8_E4M3FN> { using T = AccFn8; };
+
+// Two e4m3fn codes (low 16 bits) -> their values as f16x2, exactly.
+__device__ __forceinline__ uint32_t fn2_to_h2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// f16x2 -> two e4m3fn codes (low 16 bits): round to nearest even, saturating.
+__device__ __forceinline__ uint32_t h2_to_fn2(uint32_t h2) {
+    __half2_raw r;
+    r.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+    r.y = static_cast<unsigned short>(h2 >> 16);
+    return __nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ uint32_t hadd2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void fn8_seed(AccFn8& a, const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+    for (int i = 0; i < 4; ++i) {
+        a.h[2 * i] = fn2_to_h2(w[i]);
+        a.h[2 * i + 1] = fn2_to_h2(w[i] >> 16);
+    }
+}
+__device__ __forceinline__ void fn8_add(AccFn8& a, const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a.h[2 * i] = fn2_to_h2(h2_to_fn2(hadd2_rn(a.h[2 * i], fn2_to_h2(w[i]))));
+        a.h[2 * i + 1] = fn2_to_h2(h2_to_fn2(hadd2_rn(a.h[2 * i + 1], fn2_to_h2(w[i] >> 16))));
+    }
+}
+__device__ __forceinline__ uint4 fn8_round(const AccFn8& a) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = h2_to_fn2(a.h[2 * i]) | (h2_to_fn2(a.h[2 * i + 1]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int DT, int ACC> __device__ __forceinline__ void seed(typename AccOf<DT, ACC>::T& a, const uint4& v) {
+    if constexpr (NativeFn8<DT, ACC>::k) {
+        fn8_seed(a, v);
+    } else if constexpr (ScaledB15<DT, ACC>::k) {
+        acc_seed_scaled(a, v);
+    } else {
+        acc_seed<DT>(a, v);
+        if constexpr (ACC != SAR_FP32) {
+#pragma unroll
+            for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+        }
     }
 }
 
-template <int DT, int ACC> __device__ __forceinline__ void add(Acc<DT>& a, const uint4& v) {
-    acc_add<DT>(a, v);
-    if constexpr (ACC != SAR_FP32) {
+template <int DT, int ACC> __device__ __forceinline__ void add(typename AccOf<DT, ACC>::T& a, const uint4& v) {
+    if constexpr (NativeFn8<DT, ACC>::k) {
+        fn8_add(a, v);
+    } else if constexpr (ScaledB15<DT, ACC>::k) {
+        acc_add_scaled(a, v);
+    } else {
+        acc_add<DT>(a, v);
+        if constexpr (ACC != SAR_FP32) {
 #pragma unroll
-        for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+            for (int e = 0; e < Elem<DT>::kVE; ++e) a.v[e] = round_acc<ACC>(a.v[e]);
+        }
     }
+}
+
+template <int DT, int ACC> __device__ __forceinline__ uint4 round_out(const typename AccOf<DT, ACC>::T& a) {
+    if constexpr (NativeFn8<DT, ACC>::k) return fn8_round(a);
+    else if constexpr (ScaledB15<DT, ACC>::k) return acc_round_scaled(a);
+    else return acc_round<DT>(a);
 }
 
 template <int MODE, int NR>
@@ -110,7 +193,7 @@ __device__ __forceinline__ void reduce_element(const RankPtrs& p, int n_rt, int 
 // n_rt are skipped.
 template <int DT, int NR, int ACC, int WIN, int U>
 __device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k0, const size_t (&v)[U],
-                                              Acc<DT> (&acc)[U]) {
+                                              typename AccOf<DT, ACC>::T (&acc)[U]) {
     uint4 x[WIN][U];
 #pragma unroll
     for (int k = 0; k < WIN; ++k)
@@ -131,11 +214,11 @@ __device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k
 template <int DT, int NR, int MODE, int ACC>
 __device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r, size_t v) {
     constexpr int WIN = Shape<NR>::kWin;
-    Acc<DT> acc[1];
+    typename AccOf<DT, ACC>::T acc[1];
     const size_t vv[1] = {v};
 #pragma unroll 1
     for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, 1>(p, n_rt, k0, vv, acc);
-    store_vector<MODE, NR>(p, n_rt, r, v, acc_round<DT>(acc[0]));
+    store_vector<MODE, NR>(p, n_rt, r, v, round_out<DT, ACC>(acc[0]));
 }
 
 // Vector kernel: grid = (tiles of chunk r, nranks).  Requires every buffer to
@@ -163,12 +246,12 @@ vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
             size_t v[UNROLL];
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) v[u] = vbase + t0 + u * kThreads + threadIdx.x;
-            Acc<DT> acc[UNROLL];
+            typename AccOf<DT, ACC>::T acc[UNROLL];
             // Windows of 8 ranks run as a loop (one window for up to 8 ranks).
 #pragma unroll 1
             for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, UNROLL>(p, n_rt, k0, v, acc);
 #pragma unroll
-            for (int u = 0; u < UNROLL; ++u) store_vector<MODE, NR>(p, n_rt, r, v[u], acc_round<DT>(acc[u]));
+            for (int u = 0; u < UNROLL; ++u) store_vector<MODE, NR>(p, n_rt, r, v[u], round_out<DT, ACC>(acc[u]));
         } else {
             // Edge tile: whole vectors one at a time, then the partial vector
             // (only the last chunk can end inside a vector) element by element.

@@ -8,7 +8,8 @@
 // never flushed; this library is built without fast-math or ftz), and the sum
 // is rounded once to the element type: the hardware cvt.rn conversions for
 // bf16, fp16 and e4m3fn (satfinite), software round-to-nearest-even for the
-// e4m3b15 type, which has no hardware conversion.
+// e4m3b15 type, which has no hardware conversion (the rsag vector path instead
+// runs e4m3b15 on the e4m3fn conversions, exactly, as described below).
 #pragma once
 
 #include <cstddef>
@@ -146,6 +147,69 @@ template <> __device__ __forceinline__ uint32_t narrow_word<SAR_FP8_E4M3B15>(con
            (f32_to_e4m3b15(x[3]) << 24);
 }
 
+// ---------------------------------------------------------------------------
+// e4m3b15 on the e4m3fn hardware conversions (the vector path with a binary32
+// accumulator).  The two formats have the same fields and differ in the bias
+// (15 and 7) and in exponent field 15 (infinity and NaN in e4m3b15; 256..448
+// and, with fraction 7, NaN in e4m3fn).  So a finite e4m3b15 code read as
+// e4m3fn is its value times 2^8 exactly, subnormals included, and 2^8 times
+// the e4m3b15 grid is the e4m3fn grid up to 240 = 2^8 * 0.9375.
+//   * Sums.  Every e4m3b15 value is a multiple of 2^-17 of magnitude at most
+//     0.9375, so a partial sum of up to 136 of them is a multiple of 2^-17
+//     below 2^7 and exact in binary32 (24 bits), scaled or not:
+//     the scaled sum is 2^8 times the sum, bit for bit, and infinities and
+//     NaN combine the same way once the special codes are fixed up.
+//   * Rounding.  Clamping 2^8 s to +-256 (NaN kept) and converting with the
+//     saturating e4m3fn cvt rounds 2^8 s to the e4m3fn grid, which is 2^8
+//     times rounding s to the e4m3b15 grid.  |s| >= 0.96875 (the overflow
+//     threshold) lands on 256, whose code 0x78 is e4m3b15 infinity, and NaN
+//     gives 0x7F.
+// ---------------------------------------------------------------------------
+
+static_assert(SAR_MAX_RANKS <= 136, "e4m3b15 sums on the e4m3fn path are exact only up to 136 ranks");
+
+// True when any of the 16 codes has exponent field 15: (code & 0x7F) + 8
+// carries into bit 7 exactly then, and never into the next byte.
+__device__ __forceinline__ bool e4m3b15_vec_has_special(const uint4& v) {
+    const uint32_t t = ((v.x & 0x7F7F7F7Fu) + 0x08080808u) | ((v.y & 0x7F7F7F7Fu) + 0x08080808u) |
+                       ((v.z & 0x7F7F7F7Fu) + 0x08080808u) | ((v.w & 0x7F7F7F7Fu) + 0x08080808u);
+    return (t & 0x80808080u) != 0u;
+}
+
+// 16 codes -> 2^8 times their values.  The e4m3fn reading of exponent field
+// 15 is 256 (fraction 0: infinity here), 288..448 or NaN (fractions 1..7: NaN
+// here); every other code reads at most 240.
+__device__ __forceinline__ void e4m3b15_widen_scaled(const uint4& v, float* y) {
+    widen_word<SAR_FP8_E4M3FN>(v.x, y + 0);
+    widen_word<SAR_FP8_E4M3FN>(v.y, y + 4);
+    widen_word<SAR_FP8_E4M3FN>(v.z, y + 8);
+    widen_word<SAR_FP8_E4M3FN>(v.w, y + 12);
+    if (e4m3b15_vec_has_special(v)) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float a = fabsf(y[e]);
+            const float inf = copysignf(__int_as_float(0x7F800000), y[e]);
+            y[e] = a == 256.0f ? inf : (a > 256.0f ? __int_as_float(0x7FFFFFFF) : y[e]);
+        }
+    }
+}
+
+// max(min(y, 256), -256), with NaN propagated (min.NaN / max.NaN).
+__device__ __forceinline__ float clamp_256_keep_nan(float y) {
+    const float hi = 256.0f, lo = -256.0f;
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(y), "f"(hi));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(r), "f"(lo));
+    return r;
+}
+
+// 2^8 times binary32 sums -> one word of 4 e4m3b15 codes.
+__device__ __forceinline__ uint32_t e4m3b15_narrow_scaled_word(const float* y) {
+    const float c[4] = {clamp_256_keep_nan(y[0]), clamp_256_keep_nan(y[1]), clamp_256_keep_nan(y[2]),
+                        clamp_256_keep_nan(y[3])};
+    return narrow_word<SAR_FP8_E4M3FN>(c);
+}
+
 // Elements per 32-bit word.
 template <int DT> struct PerWord { static constexpr int kN = 4 / Elem<DT>::kSize; };
 
@@ -184,6 +248,22 @@ template <int DT> __device__ __forceinline__ uint4 acc_round(const Acc<DT>& a) {
     r.z = narrow_word<DT>(a.v + 2 * W);
     r.w = narrow_word<DT>(a.v + 3 * W);
     return r;
+}
+
+// The same three steps for e4m3b15 with the accumulator holding 2^8 times
+// the binary32 sums (see e4m3b15_widen_scaled).
+__device__ __forceinline__ void acc_seed_scaled(Acc<SAR_FP8_E4M3B15>& a, const uint4& v) {
+    e4m3b15_widen_scaled(v, a.v);
+}
+__device__ __forceinline__ void acc_add_scaled(Acc<SAR_FP8_E4M3B15>& a, const uint4& v) {
+    float y[16];
+    e4m3b15_widen_scaled(v, y);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) a.v[e] = __fadd_rn(a.v[e], y[e]);
+}
+__device__ __forceinline__ uint4 acc_round_scaled(const Acc<SAR_FP8_E4M3B15>& a) {
+    return make_uint4(e4m3b15_narrow_scaled_word(a.v + 0), e4m3b15_narrow_scaled_word(a.v + 4),
+                      e4m3b15_narrow_scaled_word(a.v + 8), e4m3b15_narrow_scaled_word(a.v + 12));
 }
 
 // ---------------------------------------------------------------------------

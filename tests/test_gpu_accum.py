@@ -89,3 +89,20 @@ def test_full_size_e4m3fn_workload_sampled(sar, acc):
     for j in range(wl.nranks):
         assert np.array_equal(dout[j][tidx].cpu().numpy(), want)
         assert torch.equal(dout[j], dout[0])
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_native_e4m3fn_every_pair(sar, n):
+    """Native e4m3fn accumulation over every ordered pair of codes (NaN
+    included), then, with 3 ranks, a third code on top of every rounded pair
+    sum: each step R(acc + x) on the vector path."""
+    a = np.repeat(np.arange(256, dtype=np.uint8), 256)
+    b = np.tile(np.arange(256, dtype=np.uint8), 256)
+    ins = [a, b]
+    if n == 3:
+        ins.append(np.roll(b, 17) ^ 0x80)
+    want = oracle.allreduce_accum(ins, "e4m3fn", "e4m3fn")[0]
+    _, gout = _run(sar, ins, "e4m3fn", "e4m3fn")
+    for g in gout:
+        assert_same(g.codes("e4m3fn"), want, "e4m3fn")
+        assert g.guards_intact()

@@ -126,6 +126,69 @@ def test_nan_and_infinity_inputs(sar, dt):
     _check(gin, gout, ins, want, dt)
 
 
+
+FP8 = ["e4m3fn", "e4m3b15"]
+
+
+def _finite_fp8(rng, dt, n):
+    c = rng.integers(0, 256, n, dtype=np.uint8)
+    special = (c & 0x78) == 0x78 if dt == "e4m3b15" else (c & 0x7F) == 0x7F
+    c[special] &= 0x87                       # exponent field 0: a finite code
+    return c
+
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("dt", FP8)
+def test_every_pair_of_fp8_codes(sar, dt, algo):
+    """Two ranks holding every ordered pair of codes, infinity and NaN codes
+    included: every two-term sum and its one rounding, on the vector path."""
+    a = np.repeat(np.arange(256, dtype=np.uint8), 256)
+    b = np.tile(np.arange(256, dtype=np.uint8), 256)
+    ins = [a, b]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, algo)
+    _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("dt", FP8)
+def test_one_special_code_in_a_vector(sar, dt):
+    """One infinity, NaN or extreme code among finite codes, at every lane of
+    a 16-byte vector and in every rank; for e4m3b15 also +inf and -inf meeting
+    in one lane (NaN)."""
+    rng = np.random.default_rng(21)
+    n = 4
+    specials = {"e4m3b15": [0x78, 0xF8, 0x79, 0x7F, 0xFF, 0x77, 0xF7],
+                "e4m3fn": [0x7F, 0xFF, 0x7E, 0xFE]}[dt]
+    cases = [(r, lane, c) for r in range(n) for lane in range(16) for c in specials]
+    nvec = len(cases) + 16 + 1
+    ins = [_finite_fp8(rng, dt, 16 * nvec) for _ in range(n)]
+    for i, (r, lane, c) in enumerate(cases):
+        ins[r][16 * i + lane] = c
+    if dt == "e4m3b15":
+        for lane in range(16):
+            v = 16 * (len(cases) + lane)
+            ins[0][v + lane], ins[2][v + lane] = 0x78, 0xF8
+    want = oracle.allreduce(ins, dt)[0]
+    for algo in (0, 1):
+        gin, gout = _run(sar, ins, dt, algo)
+        _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("dt", FP8)
+def test_extreme_sums_at_32_ranks(sar, dt):
+    """32 ranks of the largest finite, the smallest subnormal and signed zero
+    codes: overflow (to infinity or, for e4m3fn, saturation) and the exact
+    sums of subnormals."""
+    top = 0x77 if dt == "e4m3b15" else 0x7E
+    row = np.array([top, top | 0x80, 0x01, 0x81, 0x00, 0x80, 0x08, 0x88] * 4, np.uint8)
+    ins = [row.copy() for _ in range(32)]
+    ins[5][5] = 0x00                                   # one +0 among 31 -0: the sum is +0
+    want = oracle.allreduce(ins, dt)[0]
+    for algo in (0, 1):
+        gin, gout = _run(sar, ins, dt, algo)
+        _check(gin, gout, ins, want, dt)
+
+
 def test_rank_order_is_fixed(sar):
     """In binary32 ((2^24 + 1) - 2^24) + 1 = 1, while any other grouping or
     the reversed order gives 2."""
@@ -217,14 +280,15 @@ def _sample_indices(count, n, dt, rng):
     return np.unique(np.concatenate(idx))
 
 
-FULL = [W.C1, W.C2, W.C3[-1], W.C4, W.C4_STRESS]
+FULL = [W.C1, W.C2, W.C3[-1], W.C4, W.C4_STRESS, W.C4_B15]
 
 
 @pytest.mark.parametrize("wl", FULL, ids=[w.name for w in FULL])
 def test_full_size_workload_sampled(sar, wl):
     dt, n, count = wl.dtype, wl.nranks, wl.count
     ins = wl.inputs()
-    tdt = {"bf16": torch.int16, "fp16": torch.int16, "fp32": torch.int32, "e4m3fn": torch.uint8}[dt]
+    tdt = {"bf16": torch.int16, "fp16": torch.int16, "fp32": torch.int32, "e4m3fn": torch.uint8,
+           "e4m3b15": torch.uint8}[dt]
     din = [torch.from_numpy(x.view(np.int16) if ESIZE[dt] == 2 else x.view(np.int32) if dt == "fp32" else x)
            .cuda() for x in ins]
     dout = [torch.empty_like(din[0]) for _ in range(n)]
