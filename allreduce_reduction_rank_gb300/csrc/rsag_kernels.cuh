@@ -225,7 +225,8 @@ __device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r
 // be 16-byte aligned; chunk is a multiple of the vector length.
 template <int DT, int NR, int MODE, int ACC>
 __global__ void __launch_bounds__(kThreads)
-vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
+vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
+    if (pdl) pdl_wait();
     constexpr int VE = Elem<DT>::kVE;
     constexpr int WIN = Shape<NR>::kWin;
     constexpr int UNROLL = UnrollOf<DT, NR>::k;
@@ -273,7 +274,8 @@ vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
 // serves every rank count.
 template <int DT, int MODE, int ACC>
 __global__ void __launch_bounds__(kThreads)
-scalar_kernel(const RankPtrs p, int nranks, size_t count, size_t chunk) {
+scalar_kernel(const RankPtrs p, int nranks, size_t count, size_t chunk, bool pdl) {
+    if (pdl) pdl_wait();
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
     if (begin >= count) return;
@@ -298,7 +300,8 @@ cudaError_t launch_vec(const RankPtrs& p, int nranks, size_t count, size_t chunk
     constexpr int VE = Elem<DT>::kVE;
     const size_t tile = static_cast<size_t>(kThreads) * UnrollOf<DT, NR>::k;
     const dim3 grid(grid_x((chunk + VE - 1) / VE, tile, kMaxGridX), nranks);
-    vec_kernel<DT, NR, MODE, ACC><<<grid, kThreads, 0, s>>>(p, nranks, count, chunk);
+    const bool short_call = 2 * static_cast<size_t>(nranks) * count * Elem<DT>::kSize <= kShortLaunchBytes;
+    launch_kernel(short_call, vec_kernel<DT, NR, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
     return cudaGetLastError();
 }
 
@@ -306,7 +309,8 @@ template <int DT, int MODE, int ACC>
 cudaError_t launch_ranks(int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec, cudaStream_t s) {
     if (!vec) {
         const dim3 grid(grid_x(chunk, kThreads, kScalarGridX), nranks);
-        scalar_kernel<DT, MODE, ACC><<<grid, kThreads, 0, s>>>(p, nranks, count, chunk);
+        const bool short_call = 2 * static_cast<size_t>(nranks) * count * Elem<DT>::kSize <= kShortLaunchBytes;
+        launch_kernel(short_call, scalar_kernel<DT, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
         return cudaGetLastError();
     }
     switch (nranks) {
