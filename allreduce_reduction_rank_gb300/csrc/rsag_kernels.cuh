@@ -29,14 +29,27 @@ namespace sar {
 namespace rsag {
 
 // Loads in flight per thread: all ranks for up to 8 ranks (x UNROLL vectors),
-// windows of 8 ranks above that to bound register use.  NR = 0 is the kernel
-// for a rank count known only at run time (any count up to SAR_MAX_RANKS):
-// windows of 4 predicated loads.
+// windows of 8 ranks above that to bound register use.  NR > 0 is a kernel for
+// exactly NR ranks (loops unrolled at compile time); NR < 0 is a kernel for at
+// most -NR ranks, the count known only at run time (any count up to
+// SAR_MAX_RANKS outside the exact ones), with predicated loads.  Its class
+// keeps enough loads in flight for the counts it serves: -4 for 3 ranks (4
+// vectors per thread), -8 for 5 to 7 ranks (one window of 8), -32 for 9 and
+// more (windows of 4, 2 vectors per thread).  One shape for every count
+// measured 85-91% of the copy peak at 3 to 6 ranks.
 template <int NR> struct Shape {
     static constexpr int kWin = NR < 8 ? NR : 8;
     static constexpr int kUnroll = NR <= 2 ? 4 : (NR <= 8 ? 2 : 1);
 };
-template <> struct Shape<0> {
+template <> struct Shape<-4> {
+    static constexpr int kWin = 4;
+    static constexpr int kUnroll = 4;
+};
+template <> struct Shape<-8> {
+    static constexpr int kWin = 8;
+    static constexpr int kUnroll = 2;
+};
+template <> struct Shape<-32> {
     static constexpr int kWin = 4;
     static constexpr int kUnroll = 2;
 };
@@ -188,36 +201,58 @@ __device__ __forceinline__ void reduce_element(const RankPtrs& p, int n_rt, int 
     }
 }
 
+// A 16-byte vector of -0 codes: -0 is the exact identity of the
+// round-to-nearest-even add (x + -0 = x for every x, +0, -0, infinities and
+// NaN included), and of a rounding into any accumulator, since an accumulator
+// value is representable there.
+template <int DT> __device__ __forceinline__ uint4 neg_zero_vec() {
+    constexpr uint32_t w = Elem<DT>::kSize == 4 ? 0x80000000u : (Elem<DT>::kSize == 2 ? 0x80008000u : 0x80808080u);
+    return make_uint4(w, w, w, w);
+}
+
 // Ranks [k0, k0 + WIN) of vectors v[0..U): loads first, then the in-order adds
-// (the first rank seeds the accumulator).  With NR == 0 the ranks at or past
-// n_rt are skipped.
+// (the first rank seeds the accumulator).  With NR < 0 a rank at or past n_rt
+// is not loaded and adds a vector of -0 instead, so the adds need no branches.
 template <int DT, int NR, int ACC, int WIN, int U>
 __device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k0, const size_t (&v)[U],
                                               typename AccOf<DT, ACC>::T (&acc)[U]) {
     uint4 x[WIN][U];
 #pragma unroll
+    for (int k = 0; k < WIN; ++k) {
+        const bool live = NR > 0 || k0 + k < n_rt;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            x[k][u] = live ? ld_stream(static_cast<const uint4*>(p.in[k0 + k]) + v[u]) : neg_zero_vec<DT>();
+    }
+#pragma unroll
     for (int k = 0; k < WIN; ++k)
-        if (NR > 0 || k0 + k < n_rt)
 #pragma unroll
-            for (int u = 0; u < U; ++u) x[k][u] = ld_stream(static_cast<const uint4*>(p.in[k0 + k]) + v[u]);
-#pragma unroll
-    for (int k = 0; k < WIN; ++k)
-        if (NR > 0 || k0 + k < n_rt)
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (k0 + k == 0) seed<DT, ACC>(acc[u], x[k][u]);
-                else add<DT, ACC>(acc[u], x[k][u]);
-            }
+        for (int u = 0; u < U; ++u) {
+            if (k0 + k == 0) seed<DT, ACC>(acc[u], x[k][u]);
+            else add<DT, ACC>(acc[u], x[k][u]);
+        }
+}
+
+// Every rank window of vectors v[0..U).  A class whose ranks fit one window
+// runs it once at k0 = 0, so its rank pointers are indexed at compile time.
+template <int DT, int NR, int ACC, int U>
+__device__ __forceinline__ void reduce_ranks(const RankPtrs& p, int n_rt, const size_t (&v)[U],
+                                             typename AccOf<DT, ACC>::T (&acc)[U]) {
+    constexpr int WIN = Shape<NR>::kWin;
+    if constexpr (NR < 0 && -NR <= WIN) {
+        reduce_window<DT, NR, ACC, WIN, U>(p, n_rt, 0, v, acc);
+    } else {
+#pragma unroll 1
+        for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, U>(p, n_rt, k0, v, acc);
+    }
 }
 
 // One full 16-byte vector (index v counted from the start of the buffers).
 template <int DT, int NR, int MODE, int ACC>
 __device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r, size_t v) {
-    constexpr int WIN = Shape<NR>::kWin;
     typename AccOf<DT, ACC>::T acc[1];
     const size_t vv[1] = {v};
-#pragma unroll 1
-    for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, 1>(p, n_rt, k0, vv, acc);
+    reduce_ranks<DT, NR, ACC, 1>(p, n_rt, vv, acc);
     store_vector<MODE, NR>(p, n_rt, r, v, round_out<DT, ACC>(acc[0]));
 }
 
@@ -228,7 +263,6 @@ __global__ void __launch_bounds__(kThreads)
 vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
     if (pdl) pdl_wait();
     constexpr int VE = Elem<DT>::kVE;
-    constexpr int WIN = Shape<NR>::kWin;
     constexpr int UNROLL = UnrollOf<DT, NR>::k;
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
@@ -249,8 +283,7 @@ vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
             for (int u = 0; u < UNROLL; ++u) v[u] = vbase + t0 + u * kThreads + threadIdx.x;
             typename AccOf<DT, ACC>::T acc[UNROLL];
             // Windows of 8 ranks run as a loop (one window for up to 8 ranks).
-#pragma unroll 1
-            for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, UNROLL>(p, n_rt, k0, v, acc);
+            reduce_ranks<DT, NR, ACC, UNROLL>(p, n_rt, v, acc);
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) store_vector<MODE, NR>(p, n_rt, r, v[u], round_out<DT, ACC>(acc[u]));
         } else {
@@ -321,8 +354,11 @@ cudaError_t launch_ranks(int nranks, const RankPtrs& p, size_t count, size_t chu
     case 16: return launch_vec<DT, 16, MODE, ACC>(p, 16, count, chunk, s);
     case 32: return launch_vec<DT, 32, MODE, ACC>(p, 32, count, chunk, s);
     default:
+        // any other count: a kernel for the smallest class that holds it
         if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
-        return launch_vec<DT, 0, MODE, ACC>(p, nranks, count, chunk, s);   // any other count
+        if (nranks <= 4) return launch_vec<DT, -4, MODE, ACC>(p, nranks, count, chunk, s);
+        if (nranks <= 8) return launch_vec<DT, -8, MODE, ACC>(p, nranks, count, chunk, s);
+        return launch_vec<DT, -32, MODE, ACC>(p, nranks, count, chunk, s);
     }
 }
 

@@ -27,7 +27,7 @@ namespace sar {
 constexpr int kThreads = 256;
 
 // Kernels take the rank count as a template parameter NR, unrolled at compile
-// time for 1, 2, 4, 8, 16 and 32 ranks; NR == 0 is the variant for any other
+// time for 1, 2, 4, 8, 16 and 32 ranks; NR <= 0 marks a variant for any other
 // count, passed at run time.
 template <int NR> __device__ __forceinline__ int ranks(int n_rt) { return NR > 0 ? NR : n_rt; }
 

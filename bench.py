@@ -566,6 +566,11 @@ def run_gpu(args, d: Dist) -> None:
         rows.append(rsag_row(torch, sar, W.C1, dev, stream, l2_bytes))
         for w in W.C3:
             rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes))
+        for w in W.C6:       # any rank count: reuse the 8-rank inputs, draw the ranks past 8
+            assert (w.dtype, w.count, w.dist, w.seed, w.sigma) == (wl.dtype, wl.count, wl.dist, wl.seed, wl.sigma)
+            extra = [W.rank_input(w.dist, w.seed, w.dtype, w.count, r, w.sigma) for r in range(len(ins), w.nranks)]
+            rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes, ins=(list(ins) + extra)[:w.nranks]))
+            del extra
         c4_ins = W.C4.inputs()
         rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins))
         for acc in ("e4m3fn", "fp16"):

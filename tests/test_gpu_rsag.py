@@ -189,6 +189,31 @@ def test_extreme_sums_at_32_ranks(sar, dt):
         _check(gin, gout, ins, want, dt)
 
 
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("n", [3, 5, 7, 12])
+def test_signed_zero_sums_any_rank_count(sar, dt, n):
+    """Kernels for run-time rank counts pad the missing ranks of a window with
+    -0: every mix of +0 and -0 over the ranks must still sum to +0 unless all
+    are -0 (and an all -0 element must stay -0)."""
+    rng = np.random.default_rng([n, DTYPES.index(dt)])
+    count = 4096 + 3
+    neg = {"fp32": None, "bf16": 0x8000, "fp16": 0x8000, "e4m3fn": 0x80, "e4m3b15": 0x80}[dt]
+    signs = rng.integers(0, 2, (n, count)).astype(bool)
+    signs[:, :64] = True                                  # some all -0 elements
+    ins = []
+    for r in range(n):
+        if dt == "fp32":
+            ins.append(np.where(signs[r], np.float32(-0.0), np.float32(0.0)).astype(np.float32))
+        else:
+            ins.append(np.where(signs[r], neg, 0).astype(random_codes(rng, dt, 1).dtype))
+    want = oracle.allreduce(ins, dt)[0]
+    for algo in (0, 1):
+        gin, gout = _run(sar, ins, dt, algo)
+        _check(gin, gout, ins, want, dt)
+        assert np.array_equal(gout[0].bytes(), want.view(np.uint8))
+
+
 def test_rank_order_is_fixed(sar):
     """In binary32 ((2^24 + 1) - 2^24) + 1 = 1, while any other grouping or
     the reversed order gives 2."""
@@ -280,7 +305,7 @@ def _sample_indices(count, n, dt, rng):
     return np.unique(np.concatenate(idx))
 
 
-FULL = [W.C1, W.C2, W.C3[-1], W.C4, W.C4_STRESS, W.C4_B15]
+FULL = [W.C1, W.C2, W.C3[-1], W.C4, W.C4_STRESS, W.C4_B15, W.C6[3], W.C6[4]]
 
 
 @pytest.mark.parametrize("wl", FULL, ids=[w.name for w in FULL])

@@ -191,3 +191,7 @@ C4_B15 = Workload("rsag_8x16MiB_e4m3b15", 8, "e4m3b15", 16 * MiB, "normal", 2, 0
 C5 = [Workload(f"ll_8x{s // KiB}KiB_{dt}", 8, dt, s // ESIZE[dt], "uniform", 3, algo="ll")
       for dt in ("fp32", "bf16") for s in (1 * KiB, 4 * KiB, 16 * KiB, 64 * KiB, 256 * KiB, 1 * MiB)]
 LL_CALLS = 1000
+# Added: rank counts outside {1, 2, 4, 8, 16, 32}, which run the kernels with a
+# rank count known only at run time, at the 64 MiB fp16 per rank of the 8-rank
+# workload (same seed and stream, so rank r < 8 holds the same codes as there).
+C6 = [Workload(f"rsag_{n}x64MiB_fp16", n, "fp16", 32 * MiB, "normal", 1, 1.0) for n in (3, 5, 6, 7, 12)]
