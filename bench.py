@@ -367,7 +367,56 @@ def cpu_baseline(ins, wl, budget_s: float = 10.0) -> dict:
     return {"value": round(bytes_ / med / GB, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {sample} elements of each of the {wl.nranks} ranks of {wl.name}, "
                       f"median of {len(runs)} runs ({t_total:.1f} s), same byte convention",
-            "us_per_call_sample": round(med * 1e6, 1), "host_cpus": os.cpu_count()}
+            "us_per_call_sample": round(med * 1e6, 1), "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu-style), or the Arm part number."""
+    parts = {"0xd4f": "Neoverse-V2", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1", "0xd49": "Neoverse-N2"}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            info = fh.read()
+    except OSError:
+        return "unknown"
+    for ln in info.splitlines():
+        if ln.lower().startswith("model name"):
+            return ln.split(":", 1)[1].strip()
+    for ln in info.splitlines():
+        if ln.startswith("CPU part"):
+            part = ln.split(":", 1)[1].strip().lower()
+            return parts.get(part, f"Arm part {part}")
+    return "unknown"
+
+
+ORACLE_SAMPLE = 1 << 20
+
+
+def oracle_per_config(reps: int = 3) -> list:
+    """The oracle as it stands, single-threaded, on every measured
+    configuration: median of `reps` runs per config, in us per call and GB/s
+    under the same byte convention.  Configurations of at most ORACLE_SAMPLE
+    elements per rank run whole; larger ones run on their first ORACLE_SAMPLE
+    elements of every rank.  LL configurations time the oracle's pack and
+    unpack-reduce together."""
+    import oracle
+    out = []
+    for w in [W.C1] + W.C3 + [W.C4, W.C4_B15] + W.C5:
+        n = min(w.count, ORACLE_SAMPLE)
+        ins = W.sample_inputs(w.dist, w.seed, w.dtype, w.count, w.nranks, np.arange(n, dtype=np.uint64), w.sigma)
+        runs = []
+        for _ in range(reps):
+            t = time.perf_counter()
+            if w.algo == "ll":
+                rc, _ = oracle.ll_unpack_reduce(oracle.ll_pack(ins, w.dtype, 1), n, w.dtype, 1)
+                assert rc == oracle.OK
+            else:
+                oracle.allreduce(ins, w.dtype)
+            runs.append(time.perf_counter() - t)
+        med = statistics.median(runs)
+        out.append({"workload": w.name, "elements_per_rank": n, "whole": n == w.count,
+                    "us_per_call": round(med * 1e6, 1),
+                    "GBps": round(2 * w.nranks * n * W.ESIZE[w.dtype] / med / GB, 4)})
+    return out
 
 
 def run_gpu(args, d: Dist) -> None:
@@ -586,6 +635,8 @@ def run_gpu(args, d: Dist) -> None:
         rows.append(convert_row(torch, sar, dev, stream))
 
     cpu = cpu_baseline(ins, wl) if d.rank == 0 and d.world == 1 and args.cpu_baseline else None
+    if cpu is not None and wl is W.C2:
+        cpu["per_config"] = oracle_per_config()
     sha = sources_sha()
     traffic = TRAFFIC["bytes_per_launch"] if (TRAFFIC["sources_sha"] == sha and wl is W.C2) else None
     clk = clocks.summary(t0 - args.settle_s - 0.1, t1)
@@ -665,7 +716,8 @@ def run_reference(args, d: Dist) -> None:
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": wl.name, "nranks": wl.nranks, "count_per_rank": wl.count,
                        "algo": "rsag (oracle: plain rank-ordered sum)", "sample": what},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": what,
+                             "cpu_model": cpu_model(), "host_cpus": os.cpu_count()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

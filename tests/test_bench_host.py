@@ -37,3 +37,19 @@ def test_source_hash_is_stable_and_tracks_the_kernel_files():
     a, b = bench.sources_sha(), bench.sources_sha()
     assert a == b and len(a) == 16
     assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.KERNEL_SOURCES)
+
+
+def test_cpu_model_is_named():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m
+
+
+def test_oracle_per_config_covers_every_measured_configuration():
+    rows = bench.oracle_per_config(reps=1)
+    names = [r["workload"] for r in rows]
+    want = [bench.W.C1] + bench.W.C3 + [bench.W.C4, bench.W.C4_B15] + bench.W.C5
+    assert names == [w.name for w in want]
+    for r, w in zip(rows, want):
+        assert r["elements_per_rank"] == min(w.count, bench.ORACLE_SAMPLE)
+        assert r["whole"] == (w.count <= bench.ORACLE_SAMPLE)
+        assert r["us_per_call"] > 0 and r["GBps"] > 0
