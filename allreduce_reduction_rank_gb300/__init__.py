@@ -95,9 +95,24 @@ def _addr(x) -> int:
     return x.data_ptr() if isinstance(x, torch.Tensor) else int(x)
 
 
+# ctypes pointer arrays by address tuple: the library copies the pointers into
+# kernel arguments and keeps nothing, so an array can serve every call with the
+# same buffers.  Bounded; cleared when full.
+_PTR_CACHE: dict = {}
+_PTR_CACHE_MAX = 256
+
+
 def _ptrs(xs):
-    xs = list(xs)
-    return (ctypes.c_void_p * max(1, len(xs)))(*[_addr(x) for x in xs]), len(xs)
+    key = tuple(xs)
+    if not key or set(map(type, key)) != {int}:
+        key = tuple(x.data_ptr() if isinstance(x, torch.Tensor) else int(x) for x in key)
+    arr = _PTR_CACHE.get(key)
+    if arr is None:
+        if len(_PTR_CACHE) >= _PTR_CACHE_MAX:
+            _PTR_CACHE.clear()
+        arr = (ctypes.c_void_p * max(1, len(key)))(*key)
+        _PTR_CACHE[key] = arr
+    return arr, len(key)
 
 
 def _stream(stream) -> int:

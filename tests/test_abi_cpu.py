@@ -150,3 +150,18 @@ def test_binding_raises_on_error(sar):
     with pytest.raises(sar.SarError) as ei:
         sar.sar_allreduce([4096] * 33, [8192] * 33, count=16, dtype="bf16", stream=0)
     assert ei.value.status == sar.SAR_ERR_UNSUPPORTED_NRANKS
+
+
+def test_binding_pointer_arrays_are_cached_and_bounded(sar):
+    import torch
+    a1, n1 = sar._ptrs([0x1000, 0x2000])
+    a2, n2 = sar._ptrs((0x1000, 0x2000))
+    assert a1 is a2 and n1 == n2 == 2 and [a1[0], a1[1]] == [0x1000, 0x2000]
+    t = torch.empty(3)
+    a3, n3 = sar._ptrs([t, 0x2000])              # tensors and raw addresses mix
+    assert n3 == 2 and [a3[0], a3[1]] == [t.data_ptr(), 0x2000]
+    for i in range(2 * sar._PTR_CACHE_MAX):
+        sar._ptrs([0x10000 + 16 * i])
+    assert len(sar._PTR_CACHE) <= sar._PTR_CACHE_MAX
+    a4, n4 = sar._ptrs([])
+    assert n4 == 0
