@@ -28,37 +28,30 @@
 namespace sar {
 namespace rsag {
 
-// Loads in flight per thread: all ranks for up to 8 ranks (x UNROLL vectors),
-// windows of 8 ranks above that to bound register use.  NR > 0 is a kernel for
-// exactly NR ranks (loops unrolled at compile time); NR < 0 is a kernel for at
-// most -NR ranks, the count known only at run time (any count up to
-// SAR_MAX_RANKS outside the exact ones), with predicated loads.  Its class
-// keeps enough loads in flight for the counts it serves: -4 for 3 ranks (4
-// vectors per thread), -8 for 5 to 7 ranks (one window of 8), -32 for 9 and
-// more (windows of 4, 2 vectors per thread).  One shape for every count
-// measured 85-91% of the copy peak at 3 to 6 ranks.
+// A thread reduces one 16-byte vector per grid-stride step: every rank's
+// load of it is issued before the first add (in windows of 8 ranks above 8,
+// to bound the registers in flight), and the many small CTAs keep the SMs
+// full.  Measured against 2 to 4 vectors per thread: equal or faster at every
+// HBM-bound size and up to 30% faster on small calls, where the grid had
+// fewer CTAs than SMs.
+//
+// NR > 0 is a kernel for exactly NR ranks (loops unrolled at compile time);
+// NR < 0 is a kernel for at most -NR ranks, the count known only at run time
+// (any count up to SAR_MAX_RANKS outside the exact ones), with predicated
+// loads: -4 serves 3 ranks, -8 serves 5 to 7 ranks (one window), -32 serves 9
+// and more (windows of 4).  A single run-time shape for every count measured
+// 85-91% of the copy peak at 3 to 6 ranks.
 template <int NR> struct Shape {
     static constexpr int kWin = NR < 8 ? NR : 8;
-    static constexpr int kUnroll = NR <= 2 ? 4 : (NR <= 8 ? 2 : 1);
 };
 template <> struct Shape<-4> {
     static constexpr int kWin = 4;
-    static constexpr int kUnroll = 4;
 };
 template <> struct Shape<-8> {
     static constexpr int kWin = 8;
-    static constexpr int kUnroll = 2;
 };
 template <> struct Shape<-32> {
     static constexpr int kWin = 4;
-    static constexpr int kUnroll = 2;
-};
-
-// Vectors per thread: the FP8 types carry 16 elements per vector and spend
-// more registers and instructions on widening, so one vector per thread keeps
-// more warps resident (measured: e4m3b15 +18%, e4m3fn +2% on 8 x 16 MiB).
-template <int DT, int NR> struct UnrollOf {
-    static constexpr int k = (DT == SAR_FP8_E4M3FN || DT == SAR_FP8_E4M3B15) ? 1 : Shape<NR>::kUnroll;
 };
 
 // x -> R_acc(x) as a binary32 value.
@@ -210,60 +203,52 @@ template <int DT> __device__ __forceinline__ uint4 neg_zero_vec() {
     return make_uint4(w, w, w, w);
 }
 
-// Ranks [k0, k0 + WIN) of vectors v[0..U): loads first, then the in-order adds
-// (the first rank seeds the accumulator).  With NR < 0 a rank at or past n_rt
-// is not loaded and adds a vector of -0 instead, so the adds need no branches.
-template <int DT, int NR, int ACC, int WIN, int U>
-__device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k0, const size_t (&v)[U],
-                                              typename AccOf<DT, ACC>::T (&acc)[U]) {
-    uint4 x[WIN][U];
+// Ranks [k0, k0 + WIN) of vector v: loads first, then the in-order adds (the
+// first rank seeds the accumulator).  With NR < 0 a rank at or past n_rt is
+// not loaded and adds a vector of -0 instead, so the adds need no branches.
+template <int DT, int NR, int ACC, int WIN>
+__device__ __forceinline__ void reduce_window(const RankPtrs& p, int n_rt, int k0, size_t v,
+                                              typename AccOf<DT, ACC>::T& acc) {
+    uint4 x[WIN];
 #pragma unroll
     for (int k = 0; k < WIN; ++k) {
         const bool live = NR > 0 || k0 + k < n_rt;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            x[k][u] = live ? ld_stream(static_cast<const uint4*>(p.in[k0 + k]) + v[u]) : neg_zero_vec<DT>();
+        x[k] = live ? ld_stream(static_cast<const uint4*>(p.in[k0 + k]) + v) : neg_zero_vec<DT>();
     }
 #pragma unroll
-    for (int k = 0; k < WIN; ++k)
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (k0 + k == 0) seed<DT, ACC>(acc[u], x[k][u]);
-            else add<DT, ACC>(acc[u], x[k][u]);
-        }
-}
-
-// Every rank window of vectors v[0..U).  A class whose ranks fit one window
-// runs it once at k0 = 0, so its rank pointers are indexed at compile time.
-template <int DT, int NR, int ACC, int U>
-__device__ __forceinline__ void reduce_ranks(const RankPtrs& p, int n_rt, const size_t (&v)[U],
-                                             typename AccOf<DT, ACC>::T (&acc)[U]) {
-    constexpr int WIN = Shape<NR>::kWin;
-    if constexpr (NR < 0 && -NR <= WIN) {
-        reduce_window<DT, NR, ACC, WIN, U>(p, n_rt, 0, v, acc);
-    } else {
-#pragma unroll 1
-        for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN, U>(p, n_rt, k0, v, acc);
+    for (int k = 0; k < WIN; ++k) {
+        if (k0 + k == 0) seed<DT, ACC>(acc, x[k]);
+        else add<DT, ACC>(acc, x[k]);
     }
 }
 
-// One full 16-byte vector (index v counted from the start of the buffers).
+// One full 16-byte vector (index v counted from the start of the buffers):
+// every rank window, one rounding, the stores.  A class whose ranks fit one
+// window runs it once at k0 = 0, so its rank pointers are indexed at compile
+// time.
 template <int DT, int NR, int MODE, int ACC>
 __device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r, size_t v) {
-    typename AccOf<DT, ACC>::T acc[1];
-    const size_t vv[1] = {v};
-    reduce_ranks<DT, NR, ACC, 1>(p, n_rt, vv, acc);
-    store_vector<MODE, NR>(p, n_rt, r, v, round_out<DT, ACC>(acc[0]));
+    constexpr int WIN = Shape<NR>::kWin;
+    typename AccOf<DT, ACC>::T acc;
+    if constexpr (NR < 0 && -NR <= WIN) {
+        reduce_window<DT, NR, ACC, WIN>(p, n_rt, 0, v, acc);
+    } else {
+#pragma unroll 1
+        for (int k0 = 0; k0 < ranks<NR>(n_rt); k0 += WIN) reduce_window<DT, NR, ACC, WIN>(p, n_rt, k0, v, acc);
+    }
+    store_vector<MODE, NR>(p, n_rt, r, v, round_out<DT, ACC>(acc));
 }
 
-// Vector kernel: grid = (tiles of chunk r, nranks).  Requires every buffer to
-// be 16-byte aligned; chunk is a multiple of the vector length.
+// Vector kernel: grid = (CTAs over chunk r, nranks), one vector per thread;
+// the launch covers every vector of a chunk.  Requires every buffer to be
+// 16-byte aligned; chunk is a multiple of the vector length, so only the last
+// chunk can end inside a vector, and that partial vector is reduced element
+// by element.
 template <int DT, int NR, int MODE, int ACC>
 __global__ void __launch_bounds__(kThreads)
 vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
     if (pdl) pdl_wait();
     constexpr int VE = Elem<DT>::kVE;
-    constexpr int UNROLL = UnrollOf<DT, NR>::k;
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
     if (begin >= count) return;
@@ -271,34 +256,11 @@ vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
     const size_t vbase = begin / VE;
     const size_t nfull = (end - begin) / VE;            // whole vectors in the chunk
     const size_t nvec = (end - begin + VE - 1) / VE;    // plus a partial one at the very end
-    const size_t tile = static_cast<size_t>(kThreads) * UNROLL;
-
-    for (size_t t0 = static_cast<size_t>(blockIdx.x) * tile; t0 < nvec;
-         t0 += static_cast<size_t>(gridDim.x) * tile) {
-        if (t0 + tile <= nfull) {
-            // Interior tile: UNROLL vectors per thread, all loads of a rank
-            // window issued before the first add.
-            size_t v[UNROLL];
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) v[u] = vbase + t0 + u * kThreads + threadIdx.x;
-            typename AccOf<DT, ACC>::T acc[UNROLL];
-            // Windows of 8 ranks run as a loop (one window for up to 8 ranks).
-            reduce_ranks<DT, NR, ACC, UNROLL>(p, n_rt, v, acc);
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) store_vector<MODE, NR>(p, n_rt, r, v[u], round_out<DT, ACC>(acc[u]));
-        } else {
-            // Edge tile: whole vectors one at a time, then the partial vector
-            // (only the last chunk can end inside a vector) element by element.
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const size_t v = t0 + u * kThreads + threadIdx.x;
-                if (v < nfull) {
-                    reduce_vector<DT, NR, MODE, ACC>(p, n_rt, r, vbase + v);
-                } else if (v < nvec) {
-                    for (size_t i = begin + v * VE; i < end; ++i) reduce_element<DT, NR, MODE, ACC>(p, n_rt, r, i);
-                }
-            }
-        }
+    const size_t v = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (v < nfull) {
+        reduce_vector<DT, NR, MODE, ACC>(p, n_rt, r, vbase + v);
+    } else if (v < nvec) {
+        for (size_t i = begin + v * VE; i < end; ++i) reduce_element<DT, NR, MODE, ACC>(p, n_rt, r, i);
     }
 }
 
@@ -331,8 +293,11 @@ constexpr size_t kScalarGridX = 8192;
 template <int DT, int NR, int MODE, int ACC>
 cudaError_t launch_vec(const RankPtrs& p, int nranks, size_t count, size_t chunk, cudaStream_t s) {
     constexpr int VE = Elem<DT>::kVE;
-    const size_t tile = static_cast<size_t>(kThreads) * UnrollOf<DT, NR>::k;
-    const dim3 grid(grid_x((chunk + VE - 1) / VE, tile, kMaxGridX), nranks);
+    // one thread per vector of a chunk: a chunk too large for one grid (over
+    // 2^31 CTAs of 256 vectors, 8 TiB per rank) is refused, never cut short
+    const size_t ctas = ((chunk + VE - 1) / VE + kThreads - 1) / kThreads;
+    if (ctas > kMaxGridX) return cudaErrorInvalidValue;
+    const dim3 grid(grid_x((chunk + VE - 1) / VE, kThreads, kMaxGridX), nranks);
     const bool short_call = 2 * static_cast<size_t>(nranks) * count * Elem<DT>::kSize <= kShortLaunchBytes;
     launch_kernel(short_call, vec_kernel<DT, NR, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
     return cudaGetLastError();
