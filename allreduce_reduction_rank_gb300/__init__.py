@@ -70,7 +70,8 @@ lib.sar_fp8_convert.argtypes = [_vp, _i32, _vp, _i32, _sz, _vp]
 lib.sar_read_device_status.argtypes = [_vp, _vp]
 lib.sar_status_string.argtypes = [_i32]
 lib.sar_status_string.restype = ctypes.c_char_p
-for _f in ("sar_allreduce", "sar_allreduce_accum", "sar_allreduce_ll_fused", "sar_allreduce_ll_writeback", "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
+for _f in ("sar_allreduce", "sar_allreduce_accum", "sar_allreduce_ll_fused", "sar_allreduce_ll_writeback",
+           "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
            "sar_allreduce_ll", "sar_allreduce_ll_noalloc", "sar_fp8_convert", "sar_read_device_status"):
     getattr(lib, _f).restype = _i32
 

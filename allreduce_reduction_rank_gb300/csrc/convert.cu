@@ -37,7 +37,9 @@ template <> __device__ __forceinline__ void quad_load<SAR_FP8_E4M3B15>(const voi
 }
 template <int DT> __device__ __forceinline__ void quad_load16(const void* base, size_t q, float (&x)[4]) {
     uint32_t a, b;
-    asm("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(static_cast<const uint2*>(base) + q));
+    asm("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+        : "=r"(a), "=r"(b)
+        : "l"(static_cast<const uint2*>(base) + q));
     widen_word<DT>(a, x);
     widen_word<DT>(b, x + 2);
 }

@@ -368,15 +368,15 @@ cudaError_t coop_launch(sar_dtype dt, int nranks, const RankPtrs& data, void* co
     a.data = data;
     for (int r = 0; r < SAR_MAX_RANKS; ++r) a.pkts[r] = r < nranks ? static_cast<uint64_t*>(pkts[r]) : nullptr;
     a.res = static_cast<uint64_t*>(res);
+#define SAR_COOP(T) coop_ranks<T, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream)
     switch (dt) {
-    case SAR_BF16: return coop_ranks<SAR_BF16, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
-    case SAR_FP16: return coop_ranks<SAR_FP16, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
-    case SAR_FP32: return coop_ranks<SAR_FP32, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
-    case SAR_FP8_E4M3FN:
-        return coop_ranks<SAR_FP8_E4M3FN, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
-    case SAR_FP8_E4M3B15:
-        return coop_ranks<SAR_FP8_E4M3B15, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, stream);
+    case SAR_BF16: return SAR_COOP(SAR_BF16);
+    case SAR_FP16: return SAR_COOP(SAR_FP16);
+    case SAR_FP32: return SAR_COOP(SAR_FP32);
+    case SAR_FP8_E4M3FN: return SAR_COOP(SAR_FP8_E4M3FN);
+    case SAR_FP8_E4M3B15: return SAR_COOP(SAR_FP8_E4M3B15);
     }
+#undef SAR_COOP
     return cudaErrorInvalidValue;
 }
 

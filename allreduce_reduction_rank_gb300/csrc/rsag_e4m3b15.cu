@@ -4,5 +4,6 @@
 #include "rsag_kernels.cuh"
 
 namespace sar {
-template cudaError_t launch_rsag_wide<SAR_FP8_E4M3B15>(RsagMode, int, const RankPtrs&, size_t, size_t, bool, cudaStream_t);
+template cudaError_t launch_rsag_wide<SAR_FP8_E4M3B15>(RsagMode, int, const RankPtrs&, size_t, size_t, bool,
+                                              cudaStream_t);
 }  // namespace sar

@@ -3,5 +3,6 @@
 #include "rsag_kernels.cuh"
 
 namespace sar {
-template cudaError_t launch_rsag_narrow<SAR_FP8_E4M3FN>(sar_dtype, int, const RankPtrs&, size_t, size_t, bool, cudaStream_t);
+template cudaError_t launch_rsag_narrow<SAR_FP8_E4M3FN>(sar_dtype, int, const RankPtrs&, size_t, size_t, bool,
+                                              cudaStream_t);
 }  // namespace sar

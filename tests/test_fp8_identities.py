@@ -69,7 +69,7 @@ def _b15_via_fn(s):
 
 def test_scaled_e4m3fn_rounding_is_e4m3b15_rounding():
     grid = np.arange(-int(1.25 * 2 ** 17), int(1.25 * 2 ** 17) + 1, dtype=np.int64)
-    s = (grid.astype(np.float64) * 2.0 ** -17).astype(np.float32)            # every sum the kernel can form near the range
+    s = (grid.astype(np.float64) * 2.0 ** -17).astype(np.float32)      # every kernel sum near the range
     halves = ((grid.astype(np.float64) + 0.5) * 2.0 ** -17).astype(np.float32)  # ties of the subnormal grid
     rng = np.random.default_rng(5)
     rand = (rng.standard_normal(200000) * np.exp2(rng.integers(-20, 8, 200000))).astype(np.float32)
