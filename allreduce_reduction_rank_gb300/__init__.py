@@ -11,7 +11,7 @@ Function names follow the C ABI: :func:`sar_allreduce`,
 :func:`sar_allreduce_accum`, :func:`sar_reduce_scatter`, :func:`sar_all_gather`,
 :func:`sar_rsag_chunk`, :func:`sar_allreduce_ll_fused`, :func:`sar_allreduce_ll_writeback`,
 :func:`sar_ll_packet_bytes`, :func:`sar_ll_pack`,
-:func:`sar_ll_unpack_reduce`, :func:`sar_allreduce_ll`,
+:func:`sar_ll_unpack_reduce`, :func:`sar_allreduce_ll`, :func:`sar_allreduce_ll_double`,
 :func:`sar_allreduce_ll_noalloc`,
 :func:`sar_fp8_convert`, :func:`sar_read_device_status`,
 :func:`sar_status_string`.
@@ -63,6 +63,7 @@ lib.sar_ll_packet_bytes.restype = _sz
 lib.sar_ll_pack.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _vp]
 lib.sar_ll_unpack_reduce.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
 lib.sar_allreduce_ll.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
+lib.sar_allreduce_ll_double.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _u64, _vp, _vp]
 lib.sar_allreduce_ll_fused.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _vp, _u64, _vp, _vp]
 lib.sar_allreduce_ll_writeback.argtypes = [_vpp, _vpp, _vpp, _vp, _i32, _sz, _i32, _u32, _vp, _i32, _u64, _vp, _vp]
 lib.sar_allreduce_ll_noalloc.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u64, _vp, _vp]
@@ -72,7 +73,8 @@ lib.sar_status_string.argtypes = [_i32]
 lib.sar_status_string.restype = ctypes.c_char_p
 for _f in ("sar_allreduce", "sar_allreduce_accum", "sar_allreduce_ll_fused", "sar_allreduce_ll_writeback",
            "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
-           "sar_allreduce_ll", "sar_allreduce_ll_noalloc", "sar_fp8_convert", "sar_read_device_status"):
+           "sar_allreduce_ll", "sar_allreduce_ll_double", "sar_allreduce_ll_noalloc", "sar_fp8_convert",
+           "sar_read_device_status"):
     getattr(lib, _f).restype = _i32
 
 
@@ -207,6 +209,23 @@ def sar_allreduce_ll(ins, outs, pkts, epoch: int, status, max_spins: int = 1 << 
     ppk, _ = _ptrs(pkts)
     _check(lib.sar_allreduce_ll(pin, pout, ppk, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), epoch,
                                 max_spins, _addr(status), _stream(stream)))
+
+
+def ll_double_packet_bytes(count: int, dtype) -> int:
+    """Bytes of one rank's double-buffered packet scratch: two halves of
+    sar_ll_packet_bytes rounded up to 16 bytes."""
+    return 2 * ((sar_ll_packet_bytes(count, dtype) + 15) // 16 * 16)
+
+
+def sar_allreduce_ll_double(ins, outs, pkts, epoch: int, status, max_spins: int = 1 << 20, count=None, dtype=None,
+                            stream=None) -> None:
+    """sar_allreduce_ll on a double-buffered scratch: half (epoch & 1) of each
+    pkts[r] (see ll_double_packet_bytes)."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    ppk, _ = _ptrs(pkts)
+    _check(lib.sar_allreduce_ll_double(pin, pout, ppk, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), epoch,
+                                       max_spins, _addr(status), _stream(stream)))
 
 
 def sar_allreduce_ll_fused(ins, outs, pkts, status, epoch: int = 0, epoch_ctrl=None, max_spins: int = 1 << 20,

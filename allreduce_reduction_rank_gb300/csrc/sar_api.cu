@@ -117,6 +117,38 @@ sar_status check_status_args(uint64_t max_spins, const int32_t* d_status) {
     return SAR_OK;
 }
 
+// The LL allreduce (pack, then poll/unpack/reduce) on the packet scratch
+// `pkts`; with `two_halves` the scratch is double-buffered and the call uses
+// half (epoch & 1), each half being the packet bytes rounded up to 16.
+sar_status allreduce_ll(const void* const* in, void* const* out, void* const* pkts, int nranks, size_t count,
+                        sar_dtype dtype, uint32_t epoch, uint64_t max_spins, int32_t* d_status, sar_stream_t stream,
+                        bool two_halves) {
+    bool launch = false, in16 = false, out16 = false;
+    sar_status st = check_ll(in, pkts, nranks, count, dtype, epoch, &launch, &in16);
+    if (st != SAR_OK) return st;
+    if (out == nullptr) return SAR_ERR_INVALID_ARG;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (!launch) return SAR_OK;
+    if ((st = check_ll(out, pkts, nranks, count, dtype, epoch, &launch, &out16)) != SAR_OK) return st;
+    const size_t half = ((count * esize_of(dtype) + 3) / 4 * 8 + 15) / 16 * 16;
+    const size_t offset = two_halves ? (epoch & 1u) * half : 0;
+    RankPtrs pack, unpack;
+    std::memset(&pack, 0, sizeof(pack));
+    std::memset(&unpack, 0, sizeof(unpack));
+    for (int r = 0; r < nranks; ++r) {
+        void* pk = static_cast<char*>(pkts[r]) + offset;
+        pack.in[r] = in[r];
+        pack.out[r] = pk;
+        unpack.in[r] = pk;
+        unpack.out[r] = out[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = to_status(launch_ll_pack(nranks, pack, count * esize_of(dtype), epoch, in16, s));
+    if (st != SAR_OK) return st;
+    return to_status(
+        launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, true, s));
+}
+
 }  // namespace
 }  // namespace sar
 
@@ -225,27 +257,13 @@ SAR_API sar_status sar_ll_unpack_reduce(const void* const* pkts, void* const* ou
 SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, void* const* pkts, int nranks,
                                     size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
                                     int32_t* d_status, sar_stream_t stream) {
-    bool launch = false, in16 = false, out16 = false;
-    sar_status st = check_ll(in, pkts, nranks, count, dtype, epoch, &launch, &in16);
-    if (st != SAR_OK) return st;
-    if (out == nullptr) return SAR_ERR_INVALID_ARG;
-    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
-    if (!launch) return SAR_OK;
-    if ((st = check_ll(out, pkts, nranks, count, dtype, epoch, &launch, &out16)) != SAR_OK) return st;
-    RankPtrs pack, unpack;
-    std::memset(&pack, 0, sizeof(pack));
-    std::memset(&unpack, 0, sizeof(unpack));
-    for (int r = 0; r < nranks; ++r) {
-        pack.in[r] = in[r];
-        pack.out[r] = pkts[r];
-        unpack.in[r] = pkts[r];
-        unpack.out[r] = out[r];
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = to_status(launch_ll_pack(nranks, pack, count * esize_of(dtype), epoch, in16, s));
-    if (st != SAR_OK) return st;
-    return to_status(
-        launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, true, s));
+    return allreduce_ll(in, out, pkts, nranks, count, dtype, epoch, max_spins, d_status, stream, false);
+}
+
+SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                                           size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                                           int32_t* d_status, sar_stream_t stream) {
+    return allreduce_ll(in, out, pkts, nranks, count, dtype, epoch, max_spins, d_status, stream, true);
 }
 
 SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,

@@ -256,6 +256,62 @@ def ll_row(torch, sar, wl, dev, stream, calls):
             "status_ok": ok}
 
 
+def ll_double_row(torch, sar, wl, dev, calls):
+    """LL on a double-buffered scratch shared by two streams that run at the
+    same time: stream 0 uses odd epochs (the second half), stream 1 even
+    epochs (the first half), `calls` calls each; the time is the whole span
+    over both streams, reported per call (2 * calls calls)."""
+    ins = wl.inputs()
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [[torch.empty_like(din[0]) for _ in range(wl.nranks)] for _ in range(2)]
+    nb = sar.ll_double_packet_bytes(wl.count, wl.dtype)
+    pk = [torch.zeros(nb, dtype=torch.uint8, device=dev) for _ in range(wl.nranks)]
+    st = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(2)]
+    pi, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in pk]
+    po = [[t.data_ptr() for t in dout[s]] for s in range(2)]
+
+    def run(first_epoch):
+        for i in range(calls):
+            for s in range(2):
+                sar.sar_allreduce_ll_double(pi, po[s], pp, first_epoch + 2 * i + s, st[s].data_ptr(),
+                                            count=wl.count, dtype=wl.dtype, stream=streams[s].cuda_stream)
+
+    run(1)                                   # warm-up, epochs 1 .. 2 * calls
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(streams[0])
+    streams[1].wait_event(start)
+    run(2 * calls + 1)
+    streams[0].wait_stream(streams[1])
+    end.record(streams[0])
+    end.synchronize()
+    ms = start.elapsed_time(end) / (2 * calls)
+    # The same calls captured in one CUDA graph (stream 1 forked from the
+    # capturing stream and joined at the end): the GPU time, without the
+    # host's issue rate.
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=streams[0]):
+        streams[1].wait_stream(streams[0])
+        run(4 * calls + 1)
+        streams[0].wait_stream(streams[1])
+    with torch.cuda.stream(streams[0]):       # replay() launches on the current stream
+        graph.replay()
+        torch.cuda.synchronize()
+        start.record(streams[0])
+        graph.replay()
+        end.record(streams[0])
+    end.synchronize()
+    g_ms = start.elapsed_time(end) / (2 * calls)
+    del graph
+    ok = all(sar.sar_read_device_status(x.data_ptr(), streams[0].cuda_stream) == sar.SAR_OK for x in st)
+    same = all(torch.equal(dout[s][j], dout[0][0]) for s in range(2) for j in range(wl.nranks))
+    return {"workload": wl.name + "_double_two_streams", "calls": 2 * calls, "us_per_call": round(ms * 1e3, 3),
+            "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2), "graph_us_per_call": round(g_ms * 1e3, 3),
+            "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2), "status_ok": ok and same}
+
+
 def ll_fused_row(torch, sar, wl, dev, stream, calls):
     """LL in one cooperative launch: eager with host epochs 1..calls, and a
     CUDA graph of `calls` launches that take their epochs from the device
@@ -637,6 +693,8 @@ def run_gpu(args, d: Dist) -> None:
         rows.append(rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes))
         for w in W.C5:
             rows.append(ll_row(torch, sar, w, dev, stream, W.LL_CALLS))
+        for w in W.C5:
+            rows.append(ll_double_row(torch, sar, w, dev, W.LL_CALLS))
         for w in W.C5:
             rows.append(ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS))
         for w in W.C5:

@@ -216,6 +216,25 @@ SAR_API sar_status sar_allreduce_ll(const void* const* in, void* const* out, voi
                             int32_t* d_status, sar_stream_t stream);
 
 /*
+ * sar_allreduce_ll_double -- sar_allreduce_ll on a double-buffered packet
+ * scratch (mscclpp commit history, the allreduce_allpair_packet fix: the
+ * packet scratch is used in alternating halves, so a call does not overwrite
+ * packets that the previous call may still be reading).
+ *
+ * pkts[r] holds two halves of H = sar_ll_packet_bytes(count, dtype) rounded
+ * up to a multiple of 16 bytes, so 2*H bytes, 16-byte aligned, zeroed once
+ * before first use.  A call with epoch e packs into and polls half (e & 1),
+ * which starts at pkts[r] + (e & 1) * H.  Two calls whose epochs have
+ * different parity therefore touch disjoint packets and may run at the same
+ * time, for example on two streams sharing one scratch allocation; calls
+ * whose epochs have the same parity must not overlap on the GPU.  Everything
+ * else (values, status, errors) as sar_allreduce_ll.
+ */
+SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* out, void* const* pkts, int nranks,
+                                           size_t count, sar_dtype dtype, uint32_t epoch, uint64_t max_spins,
+                                           int32_t* d_status, sar_stream_t stream);
+
+/*
  * sar_allreduce_ll_fused -- the LL all-pair allreduce in one cooperative
  * launch: every block of simulated rank r packs its share of in[r] into
  * pkts[r] (the send), then polls its share of rank r's packet chunk in all N

@@ -112,6 +112,18 @@ def test_argument_errors_before_launch(sar):
     assert L.sar_allreduce_ll(ptrs2, ptrs2, ptrs2, 33, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
         sar.SAR_ERR_UNSUPPORTED_NRANKS
     assert L.sar_allreduce_ll(ptrs2, None, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4096, None) == sar.SAR_ERR_INVALID_ARG
+    # double-buffered LL: the same checks as sar_allreduce_ll
+    assert L.sar_allreduce_ll_double(ptrs2, ptrs2, ptrs2, 33, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
+        sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce_ll_double(ptrs2, None, ptrs2, 2, 16, sar.SAR_BF16, 1, 9, 4096, None) == \
+        sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce_ll_double(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 0, 9, 4096, None) == \
+        sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce_ll_double(ptrs2, ptrs2, _arr([4096, 8200]), 2, 16, sar.SAR_BF16, 2, 9, 4096, None) == \
+        sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce_ll_double(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 2, 0, 4096, None) == \
+        sar.SAR_ERR_INVALID_ARG
+    assert L.sar_allreduce_ll_double(ptrs2, ptrs2, ptrs2, 2, 0, sar.SAR_BF16, 3, 9, 4096, None) == sar.SAR_OK
     # conversion pairs: one side FP8 (e4m3fn or e4m3b15), the other fp32/fp16/bf16
     assert L.sar_fp8_convert(4096, sar.SAR_FP8_E4M3FN, 8192, sar.SAR_FP8_E4M3B15, 16, None) == \
         sar.SAR_ERR_UNSUPPORTED_DTYPE
@@ -165,3 +177,11 @@ def test_binding_pointer_arrays_are_cached_and_bounded(sar):
     assert len(sar._PTR_CACHE) <= sar._PTR_CACHE_MAX
     a4, n4 = sar._ptrs([])
     assert n4 == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16", "fp32", "e4m3fn", "e4m3b15"])
+def test_double_buffer_halves_stay_16_byte_aligned(sar, dt):
+    for count in (0, 1, 2, 3, 5, 7, 8, 9, 1023, 1024, 4097):
+        pb = sar.sar_ll_packet_bytes(count, dt)
+        total = sar.ll_double_packet_bytes(count, dt)
+        assert total % 32 == 0 and total >= 2 * pb and total - 2 * pb < 32
