@@ -16,7 +16,9 @@ namespace sar {
 namespace {
 
 // All-gather: rank r's reduced chunk in out[r] is copied to every other
-// output.  One 16-byte load, N-1 stores.
+// output.  One 16-byte load, N-1 stores; one vector per thread, the launch
+// covering every whole vector of a chunk (a grid-stride loop kept the N rank
+// pointers in registers: 78 registers and 72% of the DRAM peak at 8 ranks).
 template <int NR>
 __global__ void __launch_bounds__(kThreads)
 all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_bytes, bool pdl) {
@@ -28,8 +30,8 @@ all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_by
     const size_t vbase = begin / 16;
     const size_t nfull = (end - begin) / 16;
     const uint4* src = static_cast<const uint4*>(p.out[r]);
-    for (size_t v = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; v < nfull;
-         v += static_cast<size_t>(gridDim.x) * kThreads) {
+    const size_t v = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (v < nfull) {
         const uint4 x = ld_stream(src + vbase + v);
 #pragma unroll
         for (int j = 0; j < ranks<NR>(n_rt); ++j)
@@ -99,6 +101,8 @@ template <int NR>
 cudaError_t all_gather_dispatch(const RankPtrs& p, int nranks, size_t nbytes, size_t chunk_bytes, bool vec,
                                 bool programmatic, cudaStream_t s) {
     if (vec) {
+        // one thread per vector: a chunk too large for one grid is refused
+        if ((chunk_bytes / 16 + kThreads - 1) / kThreads > kMaxGridX) return cudaErrorInvalidValue;
         const dim3 grid(grid_x(chunk_bytes / 16, kThreads, kMaxGridX), nranks);
         launch_kernel(programmatic, all_gather_vec_kernel<NR>, grid, dim3(kThreads), s, p, nranks, nbytes,
                       chunk_bytes);

@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -677,30 +678,39 @@ def run_gpu(args, d: Dist) -> None:
     if args.rows and d.rank == 0 and wl is W.C2:
         del din, dout
         torch.cuda.empty_cache()
-        rows.append(rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=1, ins=ins))
-        rows.append(rsag_row(torch, sar, W.C1, dev, stream, l2_bytes))
-        for w in W.C3:
-            rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes))
-        for w in W.C6:       # any rank count: reuse the 8-rank inputs, draw the ranks past 8
+        c4 = {}
+
+        def c4_ins():
+            if "ins" not in c4:
+                c4["ins"] = W.C4.inputs()
+            return c4["ins"]
+
+        def any_count_row(w):      # any rank count: reuse the 8-rank inputs, draw the ranks past 8
             assert (w.dtype, w.count, w.dist, w.seed, w.sigma) == (wl.dtype, wl.count, wl.dist, wl.seed, wl.sigma)
             extra = [W.rank_input(w.dist, w.seed, w.dtype, w.count, r, w.sigma) for r in range(len(ins), w.nranks)]
-            rows.append(rsag_row(torch, sar, w, dev, stream, l2_bytes, ins=(list(ins) + extra)[:w.nranks]))
-            del extra
-        c4_ins = W.C4.inputs()
-        rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins))
-        for acc in ("e4m3fn", "fp16"):
-            rows.append(rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins, accum=acc))
-        rows.append(rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes))
-        for w in W.C5:
-            rows.append(ll_row(torch, sar, w, dev, stream, W.LL_CALLS))
-        for w in W.C5:
-            rows.append(ll_double_row(torch, sar, w, dev, W.LL_CALLS))
-        for w in W.C5:
-            rows.append(ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS))
-        for w in W.C5:
-            for multi in (True, False):
-                rows.append(ll_writeback_row(torch, sar, w, dev, stream, W.LL_CALLS, multi))
-        rows.append(convert_row(torch, sar, dev, stream))
+            return rsag_row(torch, sar, w, dev, stream, l2_bytes, ins=(list(ins) + extra)[:w.nranks])
+
+        # (row name, thunk): --rows-only selects rows by name
+        plan = [(wl.name + "/two_phase", lambda: rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=1, ins=ins)),
+                (W.C1.name, lambda: rsag_row(torch, sar, W.C1, dev, stream, l2_bytes))]
+        plan += [(w.name, lambda w=w: rsag_row(torch, sar, w, dev, stream, l2_bytes)) for w in W.C3]
+        plan += [(w.name, lambda w=w: any_count_row(w)) for w in W.C6]
+        plan.append((W.C4.name, lambda: rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins())))
+        plan += [(f"{W.C4.name}/acc_{acc}",
+                  lambda acc=acc: rsag_row(torch, sar, W.C4, dev, stream, l2_bytes, ins=c4_ins(), accum=acc))
+                 for acc in ("e4m3fn", "fp16")]
+        plan.append((W.C4_B15.name, lambda: rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes)))
+        plan += [(w.name, lambda w=w: ll_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
+        plan += [(w.name + "_double", lambda w=w: ll_double_row(torch, sar, w, dev, W.LL_CALLS)) for w in W.C5]
+        plan += [(w.name + "_fused", lambda w=w: ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
+        plan += [(f"{w.name}_writeback_{'multi_dest' if m else 'own_output'}",
+                  lambda w=w, m=m: ll_writeback_row(torch, sar, w, dev, stream, W.LL_CALLS, m))
+                 for w in W.C5 for m in (True, False)]
+        plan.append(("fp8_convert", lambda: convert_row(torch, sar, dev, stream)))
+        pick = re.compile(args.rows_only) if args.rows_only else None
+        for name, run in plan:
+            if pick is None or pick.search(name):
+                rows.append(run())
 
     cpu = cpu_baseline(ins, wl) if d.rank == 0 and d.world == 1 and args.cpu_baseline else None
     if cpu is not None and wl is W.C2:
@@ -804,6 +814,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", dest="rows", action="store_false")
+    ap.add_argument("--rows-only", default=None, metavar="REGEX",
+                    help="run only the rows whose name matches (for example to profile one kernel)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
