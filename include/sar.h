@@ -78,6 +78,9 @@ typedef enum {
                             overflow rounds to inf, subnormals m/8 * 2^-14 */
 } sar_dtype;
 
+/* The LL all-pair allreduce is not a sar_algo: it needs a packet scratch, an
+ * epoch and a device status word, which sar_allreduce has no arguments for.
+ * It has its own entry points (sar_allreduce_ll and its variants below). */
 typedef enum {
     SAR_ALGO_RSAG = 0,            /* one fused kernel: reduce chunk, write to all outputs */
     SAR_ALGO_RSAG_TWO_PHASE = 1   /* reduce-scatter kernel, then all-gather kernel */
