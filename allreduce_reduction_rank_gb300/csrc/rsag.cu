@@ -7,8 +7,8 @@
 // rank reduces its 1/N chunk and writes it back to every peer.  Fused, the
 // write-back happens from registers (N*S read + N*S written); in two phases
 // the reduce-scatter writes the chunk to the owning rank's output and the
-// all-gather copies it from there to every other output (one extra S read
-// and S written).
+// all-gather copies it from there to every other output: the same N*S
+// written, plus one extra S read (the reduced chunks, read back).
 #include "sar_device.cuh"
 #include "sar_internal.h"
 
