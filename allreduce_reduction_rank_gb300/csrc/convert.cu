@@ -84,8 +84,8 @@ template <> __device__ __forceinline__ void quad_store<SAR_FP32>(void* base, siz
 
 template <int SRC, int DST>
 __global__ void __launch_bounds__(kThreads)
-convert_vec_kernel(const void* src, void* dst, size_t count, bool pdl) {
-    if (pdl) pdl_wait();
+convert_vec_kernel(const void* src, void* dst, size_t count) {
+    pdl_wait();
     const size_t nq = count / 4;
     const unsigned lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -112,8 +112,8 @@ convert_vec_kernel(const void* src, void* dst, size_t count, bool pdl) {
 
 template <int SRC, int DST>
 __global__ void __launch_bounds__(kThreads)
-convert_scalar_kernel(const void* src, void* dst, size_t count, bool pdl) {
-    if (pdl) pdl_wait();
+convert_scalar_kernel(const void* src, void* dst, size_t count) {
+    pdl_wait();
     for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; i < count;
          i += static_cast<size_t>(gridDim.x) * kThreads)
         store_elem<DST>(dst, i, load_elem<SRC>(src, i));
@@ -128,14 +128,13 @@ inline unsigned grid_x(size_t items, size_t cap) {
 
 template <int SRC, int DST>
 cudaError_t convert_launch(const void* src, void* dst, size_t count, bool vec, cudaStream_t s) {
-    const bool short_call = count * (Elem<SRC>::kSize + Elem<DST>::kSize) <= kShortLaunchBytes;
     if (vec) {
         // one warp per 32 * kUnroll quads
         const size_t warps = (count / 4 + 32 * kUnroll - 1) / (32 * kUnroll);
-        launch_kernel(short_call, convert_vec_kernel<SRC, DST>, dim3(grid_x(warps * 32 + 1, 0x7FFFFFFF)),
+        launch_kernel(convert_vec_kernel<SRC, DST>, dim3(grid_x(warps * 32 + 1, 0x7FFFFFFF)),
                       dim3(kThreads), s, src, dst, count);
     } else {
-        launch_kernel(short_call, convert_scalar_kernel<SRC, DST>, dim3(grid_x(count, 16384)), dim3(kThreads), s,
+        launch_kernel(convert_scalar_kernel<SRC, DST>, dim3(grid_x(count, 16384)), dim3(kThreads), s,
                       src, dst, count);
     }
     return cudaGetLastError();

@@ -73,8 +73,8 @@ __device__ __forceinline__ bool poll_one(const uint64_t* src, uint32_t epoch, ui
 // Pack.  p.in[r] = input, p.out[r] = packet buffer of rank r.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
-ll_pack_vec_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch, bool pdl) {
-    if (pdl) pdl_wait();
+ll_pack_vec_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
+    pdl_wait();
     const int r = blockIdx.y;
     const uint4* src = static_cast<const uint4*>(p.in[r]);
     uint64_t* dst = static_cast<uint64_t*>(p.out[r]);
@@ -100,8 +100,8 @@ ll_pack_vec_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch, bool pdl) {
 
 // Inputs that are not 16-byte aligned: one packet per thread, byte loads.
 __global__ void __launch_bounds__(kThreads)
-ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch, bool pdl) {
-    if (pdl) pdl_wait();
+ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
+    pdl_wait();
     const int r = blockIdx.y;
     const unsigned char* b = static_cast<const unsigned char*>(p.in[r]);
     uint64_t* dst = static_cast<uint64_t*>(p.out[r]);
@@ -124,8 +124,8 @@ ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch, bool pdl) 
 template <int DT, int NR>
 __global__ void __launch_bounds__(kThreads)
 ll_unpack_reduce_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t epoch,
-                        uint64_t max_spins, int32_t* status, bool vec_out, bool pdl) {
-    if (pdl) pdl_wait();
+                        uint64_t max_spins, int32_t* status, bool vec_out) {
+    pdl_wait();
     constexpr int VE = Elem<DT>::kVE;
     constexpr int EP = PerWord<DT>::kN;
     constexpr int WIN = NR == 0 ? 4 : (NR < 8 ? NR : 8);
@@ -210,30 +210,29 @@ constexpr size_t kGridCap = 65535;
 
 template <int DT, int NR>
 cudaError_t unpack_dispatch(int nranks, const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
-                            int32_t* status, bool vec_out, bool after_pack, cudaStream_t s) {
+                            int32_t* status, bool vec_out, cudaStream_t s) {
     const size_t nbytes = count * Elem<DT>::kSize;
     const size_t npk = (nbytes + 3) / 4, nq = (npk + 3) / 4;
     const size_t chunk_q = (nq + nranks - 1) / nranks;
     const dim3 grid(grid_x(chunk_q, kGridCap), nranks);
-    const bool pg = after_pack || 3 * static_cast<size_t>(nranks) * nbytes <= kShortLaunchBytes;
-    launch_kernel(pg, ll_unpack_reduce_kernel<DT, NR>, grid, dim3(kThreads), s, p, nranks, count, nbytes, chunk_q,
+    launch_kernel(ll_unpack_reduce_kernel<DT, NR>, grid, dim3(kThreads), s, p, nranks, count, nbytes, chunk_q,
                   epoch, max_spins, status, vec_out);
     return cudaGetLastError();
 }
 
 template <int DT>
 cudaError_t unpack_ranks(int nranks, const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
-                         int32_t* status, bool vec_out, bool after_pack, cudaStream_t s) {
+                         int32_t* status, bool vec_out, cudaStream_t s) {
     switch (nranks) {
-    case 1: return unpack_dispatch<DT, 1>(1, p, count, epoch, max_spins, status, vec_out, after_pack, s);
-    case 2: return unpack_dispatch<DT, 2>(2, p, count, epoch, max_spins, status, vec_out, after_pack, s);
-    case 4: return unpack_dispatch<DT, 4>(4, p, count, epoch, max_spins, status, vec_out, after_pack, s);
-    case 8: return unpack_dispatch<DT, 8>(8, p, count, epoch, max_spins, status, vec_out, after_pack, s);
-    case 16: return unpack_dispatch<DT, 16>(16, p, count, epoch, max_spins, status, vec_out, after_pack, s);
-    case 32: return unpack_dispatch<DT, 32>(32, p, count, epoch, max_spins, status, vec_out, after_pack, s);
+    case 1: return unpack_dispatch<DT, 1>(1, p, count, epoch, max_spins, status, vec_out, s);
+    case 2: return unpack_dispatch<DT, 2>(2, p, count, epoch, max_spins, status, vec_out, s);
+    case 4: return unpack_dispatch<DT, 4>(4, p, count, epoch, max_spins, status, vec_out, s);
+    case 8: return unpack_dispatch<DT, 8>(8, p, count, epoch, max_spins, status, vec_out, s);
+    case 16: return unpack_dispatch<DT, 16>(16, p, count, epoch, max_spins, status, vec_out, s);
+    case 32: return unpack_dispatch<DT, 32>(32, p, count, epoch, max_spins, status, vec_out, s);
     default:
         if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
-        return unpack_dispatch<DT, 0>(nranks, p, count, epoch, max_spins, status, vec_out, after_pack, s);
+        return unpack_dispatch<DT, 0>(nranks, p, count, epoch, max_spins, status, vec_out, s);
     }
 }
 
@@ -241,21 +240,20 @@ cudaError_t unpack_ranks(int nranks, const RankPtrs& p, size_t count, uint32_t e
 
 cudaError_t launch_ll_pack(int nranks, const RankPtrs& p, size_t bytes, uint32_t epoch, bool vec,
                            cudaStream_t stream) {
-    const bool short_call = 3 * static_cast<size_t>(nranks) * bytes <= kShortLaunchBytes;
     if (vec) {
         const dim3 grid(grid_x(bytes / 16 + 1, kGridCap), nranks);
-        launch_kernel(short_call, ll_pack_vec_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);
+        launch_kernel(ll_pack_vec_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);
     } else {
         const dim3 grid(grid_x((bytes + 3) / 4, kGridCap), nranks);
-        launch_kernel(short_call, ll_pack_bytes_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);
+        launch_kernel(ll_pack_bytes_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
                                     uint32_t epoch, uint64_t max_spins, int32_t* status, bool vec_out,
-                                    bool after_pack, cudaStream_t stream) {
-#define SAR_UNPACK(T) unpack_ranks<T>(nranks, p, count, epoch, max_spins, status, vec_out, after_pack, stream)
+                                    cudaStream_t stream) {
+#define SAR_UNPACK(T) unpack_ranks<T>(nranks, p, count, epoch, max_spins, status, vec_out, stream)
     switch (dt) {
     case SAR_BF16: return SAR_UNPACK(SAR_BF16);
     case SAR_FP16: return SAR_UNPACK(SAR_FP16);

@@ -115,8 +115,7 @@ extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, vo
         unpack.out[r] = out[r];
     }
     if (launch_ll_pack(nranks, pack, count * es, epoch, in16, s) != cudaSuccess) return SAR_ERR_CUDA;
-    if (launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, status, out16, true, s) !=
-        cudaSuccess)
+    if (launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, status, out16, s) != cudaSuccess)
         return SAR_ERR_CUDA;
     return SAR_OK;
 }

@@ -21,8 +21,8 @@ namespace {
 // pointers in registers: 78 registers and 72% of the DRAM peak at 8 ranks).
 template <int NR>
 __global__ void __launch_bounds__(kThreads)
-all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_bytes, bool pdl) {
-    if (pdl) pdl_wait();
+all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_bytes) {
+    pdl_wait();
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk_bytes;
     if (begin >= nbytes) return;
@@ -51,8 +51,8 @@ all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_by
 
 template <int NR>
 __global__ void __launch_bounds__(kThreads)
-all_gather_bytes_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_bytes, bool pdl) {
-    if (pdl) pdl_wait();
+all_gather_bytes_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_bytes) {
+    pdl_wait();
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk_bytes;
     if (begin >= nbytes) return;
@@ -99,16 +99,16 @@ cudaError_t rsag_dispatch(RsagMode mode, sar_dtype acc, sar_dtype dt, int nranks
 
 template <int NR>
 cudaError_t all_gather_dispatch(const RankPtrs& p, int nranks, size_t nbytes, size_t chunk_bytes, bool vec,
-                                bool programmatic, cudaStream_t s) {
+                                cudaStream_t s) {
     if (vec) {
         // one thread per vector: a chunk too large for one grid is refused
         if ((chunk_bytes / 16 + kThreads - 1) / kThreads > kMaxGridX) return cudaErrorInvalidValue;
         const dim3 grid(grid_x(chunk_bytes / 16, kThreads, kMaxGridX), nranks);
-        launch_kernel(programmatic, all_gather_vec_kernel<NR>, grid, dim3(kThreads), s, p, nranks, nbytes,
+        launch_kernel(all_gather_vec_kernel<NR>, grid, dim3(kThreads), s, p, nranks, nbytes,
                       chunk_bytes);
     } else {
         const dim3 grid(grid_x(chunk_bytes, kThreads, kScalarGridX), nranks);
-        launch_kernel(programmatic, all_gather_bytes_kernel<0>, grid, dim3(kThreads), s, p, nranks, nbytes,
+        launch_kernel(all_gather_bytes_kernel<0>, grid, dim3(kThreads), s, p, nranks, nbytes,
                       chunk_bytes);
     }
     return cudaGetLastError();
@@ -127,19 +127,18 @@ cudaError_t launch_rsag_accum(sar_dtype dt, sar_dtype acc, int nranks, const Ran
 }
 
 cudaError_t launch_all_gather(int nranks, const RankPtrs& p, size_t count, size_t esize, size_t chunk,
-                              bool vec, bool after_reduce, cudaStream_t stream) {
+                              bool vec, cudaStream_t stream) {
     const size_t nbytes = count * esize, chunk_bytes = chunk * esize;
-    const bool pg = after_reduce || static_cast<size_t>(nranks) * nbytes <= kShortLaunchBytes;
     switch (nranks) {
     case 1: return cudaSuccess;   // a single rank already holds its result
-    case 2: return all_gather_dispatch<2>(p, 2, nbytes, chunk_bytes, vec, pg, stream);
-    case 4: return all_gather_dispatch<4>(p, 4, nbytes, chunk_bytes, vec, pg, stream);
-    case 8: return all_gather_dispatch<8>(p, 8, nbytes, chunk_bytes, vec, pg, stream);
-    case 16: return all_gather_dispatch<16>(p, 16, nbytes, chunk_bytes, vec, pg, stream);
-    case 32: return all_gather_dispatch<32>(p, 32, nbytes, chunk_bytes, vec, pg, stream);
+    case 2: return all_gather_dispatch<2>(p, 2, nbytes, chunk_bytes, vec, stream);
+    case 4: return all_gather_dispatch<4>(p, 4, nbytes, chunk_bytes, vec, stream);
+    case 8: return all_gather_dispatch<8>(p, 8, nbytes, chunk_bytes, vec, stream);
+    case 16: return all_gather_dispatch<16>(p, 16, nbytes, chunk_bytes, vec, stream);
+    case 32: return all_gather_dispatch<32>(p, 32, nbytes, chunk_bytes, vec, stream);
     default:
         if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
-        return all_gather_dispatch<0>(p, nranks, nbytes, chunk_bytes, vec, pg, stream);
+        return all_gather_dispatch<0>(p, nranks, nbytes, chunk_bytes, vec, stream);
     }
 }
 

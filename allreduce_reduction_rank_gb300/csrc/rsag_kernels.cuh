@@ -246,8 +246,8 @@ __device__ __forceinline__ void reduce_vector(const RankPtrs& p, int n_rt, int r
 // by element.
 template <int DT, int NR, int MODE, int ACC>
 __global__ void __launch_bounds__(kThreads)
-vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
-    if (pdl) pdl_wait();
+vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk) {
+    pdl_wait();
     constexpr int VE = Elem<DT>::kVE;
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
@@ -269,8 +269,8 @@ vec_kernel(const RankPtrs p, int n_rt, size_t count, size_t chunk, bool pdl) {
 // serves every rank count.
 template <int DT, int MODE, int ACC>
 __global__ void __launch_bounds__(kThreads)
-scalar_kernel(const RankPtrs p, int nranks, size_t count, size_t chunk, bool pdl) {
-    if (pdl) pdl_wait();
+scalar_kernel(const RankPtrs p, int nranks, size_t count, size_t chunk) {
+    pdl_wait();
     const int r = blockIdx.y;
     const size_t begin = static_cast<size_t>(r) * chunk;
     if (begin >= count) return;
@@ -298,8 +298,7 @@ cudaError_t launch_vec(const RankPtrs& p, int nranks, size_t count, size_t chunk
     const size_t ctas = ((chunk + VE - 1) / VE + kThreads - 1) / kThreads;
     if (ctas > kMaxGridX) return cudaErrorInvalidValue;
     const dim3 grid(grid_x((chunk + VE - 1) / VE, kThreads, kMaxGridX), nranks);
-    const bool short_call = 2 * static_cast<size_t>(nranks) * count * Elem<DT>::kSize <= kShortLaunchBytes;
-    launch_kernel(short_call, vec_kernel<DT, NR, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
+    launch_kernel(vec_kernel<DT, NR, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
     return cudaGetLastError();
 }
 
@@ -307,8 +306,7 @@ template <int DT, int MODE, int ACC>
 cudaError_t launch_ranks(int nranks, const RankPtrs& p, size_t count, size_t chunk, bool vec, cudaStream_t s) {
     if (!vec) {
         const dim3 grid(grid_x(chunk, kThreads, kScalarGridX), nranks);
-        const bool short_call = 2 * static_cast<size_t>(nranks) * count * Elem<DT>::kSize <= kShortLaunchBytes;
-        launch_kernel(short_call, scalar_kernel<DT, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
+            launch_kernel(scalar_kernel<DT, MODE, ACC>, grid, dim3(kThreads), s, p, nranks, count, chunk);
         return cudaGetLastError();
     }
     switch (nranks) {

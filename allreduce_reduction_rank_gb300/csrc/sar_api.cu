@@ -146,7 +146,7 @@ sar_status allreduce_ll(const void* const* in, void* const* out, void* const* pk
     st = to_status(launch_ll_pack(nranks, pack, count * esize_of(dtype), epoch, in16, s));
     if (st != SAR_OK) return st;
     return to_status(
-        launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, true, s));
+        launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, d_status, out16, s));
 }
 
 }  // namespace
@@ -176,7 +176,7 @@ SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nr
     if (algo == SAR_ALGO_RSAG) return to_status(launch_rsag(kFused, dtype, nranks, p, count, chunk, vec, s));
     st = to_status(launch_rsag(kReduceScatter, dtype, nranks, p, count, chunk, vec, s));
     if (st != SAR_OK) return st;
-    return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), chunk, vec, true, s));
+    return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), chunk, vec, s));
 }
 
 SAR_API sar_status sar_allreduce_accum(const void* const* in, void* const* out, int nranks, size_t count,
@@ -211,7 +211,7 @@ SAR_API sar_status sar_all_gather(void* const* out, int nranks, size_t count, sa
     sar_status st = check_rsag(nullptr, out, nranks, count, dtype, false, &p, &vec, &launch);
     if (st != SAR_OK || !launch) return st;
     return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), rsag_chunk(count, nranks, dtype), vec,
-                                       false, reinterpret_cast<cudaStream_t>(stream)));
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 SAR_API size_t sar_ll_packet_bytes(size_t count, sar_dtype dtype) {
@@ -250,7 +250,7 @@ SAR_API sar_status sar_ll_unpack_reduce(const void* const* pkts, void* const* ou
         p.in[r] = pkts[r];
         p.out[r] = out[r];
     }
-    return to_status(launch_ll_unpack_reduce(dtype, nranks, p, count, epoch, max_spins, d_status, out16, false,
+    return to_status(launch_ll_unpack_reduce(dtype, nranks, p, count, epoch, max_spins, d_status, out16,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -32,14 +32,13 @@ constexpr int kThreads = 256;
 template <int NR> __device__ __forceinline__ int ranks(int n_rt) { return NR > 0 ? NR : n_rt; }
 
 // Programmatic dependent launch (sm_90 and later).  The non-cooperative
-// kernels may be launched with programmatic stream serialization
-// (launch_kernel in sar_internal.h), so a kernel can be scheduled while the
-// one before it in the stream drains.  Such a launch passes pdl = true, and
-// the kernel calls pdl_wait() before its first global-memory access: it
-// returns once the preceding kernel has completed and its writes are visible,
-// so stream order is kept exactly.  No kernel signals its dependents early
-// (griddepcontrol.launch_dependents): measured, the early signal was no
-// faster, and slower for the LL pair.
+// kernels are launched with programmatic stream serialization (launch_kernel
+// in sar_internal.h), so a kernel can be scheduled while the one before it in
+// the stream drains.  Each of them calls pdl_wait() before its first
+// global-memory access: it returns once the preceding kernel has completed and
+// its writes are visible, so stream order is kept exactly.  No kernel signals
+// its dependents early (griddepcontrol.launch_dependents): measured, the early
+// signal was no faster, and slower for the LL pair.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------

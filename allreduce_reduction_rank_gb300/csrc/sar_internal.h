@@ -13,22 +13,15 @@
 
 namespace sar {
 
-// Kernel launch.  With `programmatic`, the launch carries programmatic stream
-// serialization: the kernel may be scheduled before the previous kernel in
-// the stream has finished.  Every kernel takes a last `bool pdl` argument,
-// which this passes as `programmatic`, and then waits for the previous kernel
-// with pdl_wait() (sar_device.cuh) before touching memory, so the results are
-// the same either way.  It pays where launch latency is a large part of the
-// call: for the second kernel of a call (the all-gather after the
-// reduce-scatter, the LL unpack after the pack) and for kernels that move at
-// most kShortLaunchBytes.  Long single kernels launch as plain kernels with
-// no wait: there the wait measured about 1 us slower per call, and the
-// programmatic launch up to a few percent slower in CUDA graphs.
-constexpr size_t kShortLaunchBytes = size_t(32) << 20;
-
+// Kernel launch with programmatic stream serialization: the kernel may be
+// scheduled before the previous kernel in the stream has finished, and waits
+// for it with pdl_wait() (sar_device.cuh) before touching memory, so the
+// results are those of plain stream order.  Measured on GB300 against plain
+// launches (interleaved runs): faster at every size, e.g. 2 x 16 MiB bf16
+// 8.2 -> 6.1 us per call eager and 6.4 -> 6.0 us in a CUDA graph, 8 x 64 MiB
+// fp16 155.8 -> 153.2 us eager.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(bool programmatic, void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
-                          Args&&... args) {
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args&&... args) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -38,8 +31,8 @@ cudaError_t launch_kernel(bool programmatic, void (*kernel)(KArgs...), dim3 grid
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)..., programmatic);
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // What an rsag launch writes: the fused allreduce writes the reduced chunk to
@@ -72,19 +65,17 @@ cudaError_t launch_rsag_narrow(sar_dtype acc, int nranks, const RankPtrs& p, siz
                                cudaStream_t s);
 
 // rsag all-gather: out[j][chunk r] = out[r][chunk r], j != r (bytes).
-// after_reduce: launched directly after the reduce-scatter of the same call.
 cudaError_t launch_all_gather(int nranks, const RankPtrs& p, size_t count, size_t esize,
-                              size_t chunk, bool vec, bool after_reduce, cudaStream_t stream);
+                              size_t chunk, bool vec, cudaStream_t stream);
 
 // LL pack: pkts[r] <- packets of in[r] (p.out holds the packet buffers).
 cudaError_t launch_ll_pack(int nranks, const RankPtrs& p, size_t bytes, uint32_t epoch,
                            bool vec, cudaStream_t stream);
 
 // LL poll + unpack + reduce + write-back (p.in holds the packet buffers).
-// after_pack: launched directly after the pack of the same call.
 cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p, size_t count,
                                     uint32_t epoch, uint64_t max_spins, int32_t* status,
-                                    bool vec_out, bool after_pack, cudaStream_t stream);
+                                    bool vec_out, cudaStream_t stream);
 
 // LL send + reduce + write-back in one cooperative launch.  ctrl: optional
 // device {last epoch, arrivals}; with it the epoch is ctrl[0] + 1.
