@@ -253,6 +253,7 @@ template <int DT, int NR, int WB>
 __global__ void __launch_bounds__(kThreads)
 coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t host_epoch,
             uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16) {
+    pdl_wait();
     __shared__ uint32_t s_epoch;
     if (threadIdx.x == 0) {
         uint32_t e = host_epoch;
@@ -339,9 +340,22 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
     uint64_t ms = max_spins;
     int32_t* st = status;
     bool i16 = in16, o16 = out16;
-    void* params[] = {&args, &n_rt, &cnt, &nb, &cq, &ep, &ct, &ms, &st, &i16, &o16};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(coop_kernel<DT, NR, WB>), dim3(gx, nranks),
-                                       dim3(kThreads), params, 0, s);
+    // Cooperative (every block co-resident) and, like the other kernels,
+    // programmatic stream serialization: the kernel waits for the previous
+    // one with pdl_wait() before touching memory.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, nranks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, coop_kernel<DT, NR, WB>, args, n_rt, cnt, nb, cq, ep, ct, ms, st, i16, o16);
 }
 
 template <int DT, int WB>
