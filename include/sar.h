@@ -14,10 +14,11 @@
  *           allreduce_allpair_packet fix: send, reduce and write-back in one
  *           thread block, with flag-checked packets).
  *
- * Accumulation is always binary32 (mscclpp commit history, "Add
- * mixed-precision accumulation for allreduce": accumDtype), summed in rank
- * order 0..N-1 for every element and every output, then rounded once with
- * round-to-nearest-even.  Results are therefore reproducible bit for bit.
+ * Accumulation is binary32 (mscclpp commit history, "Add mixed-precision
+ * accumulation for allreduce": accumDtype), summed in rank order 0..N-1 for
+ * every element and every output, then rounded once with round-to-nearest-
+ * even; sar_allreduce_accum instead rounds every partial sum into a narrower
+ * accumulator.  Results are therefore reproducible bit for bit.
  *
  * Conventions shared by every entry point:
  *  - Pointer arrays (`in`, `out`, `pkts`) are HOST arrays of `nranks` DEVICE
@@ -41,6 +42,11 @@
  *    vectors; otherwise a slower element-wise kernel runs.  Results are
  *    identical either way.
  *  - A failed launch returns SAR_ERR_CUDA.
+ *  - Kernels are launched with programmatic stream serialization (programmatic
+ *    dependent launch): one may be scheduled while the work before it in the
+ *    stream drains, but it waits for that work to complete (griddepcontrol.
+ *    wait) before touching memory, so stream order and results are exactly
+ *    those of plain launches.  No library kernel signals its dependents early.
  *  - `stream` is a CUDA stream (cudaStream_t); NULL is the legacy default
  *    stream.  The current device must be the one that owns the buffers.
  */
