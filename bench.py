@@ -579,12 +579,17 @@ def run_gpu(args, d: Dist) -> None:
     torch.cuda.synchronize()
     d.barrier()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(s_in)
-    for _ in range(e2e_steps):
-        e2e_step()
-    t_end.record(s_out)
-    t_end.synchronize()
-    eager_ms = d.max(t_start.elapsed_time(t_end)) / e2e_steps
+    # best of three trials: a host-side hiccup in one trial stalls the issue of
+    # every later copy in it
+    eager_ms = float("inf")
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t_start.record(s_in)
+        for _ in range(e2e_steps):
+            e2e_step()
+        t_end.record(s_out)
+        t_end.synchronize()
+        eager_ms = min(eager_ms, d.max(t_start.elapsed_time(t_end)) / e2e_steps)
     e2e_ok = all(torch.equal(h_out[j], h_out[0]) for j in range(wl.nranks)) and \
         bool(torch.equal(h_out[0].to(dev), dout[0]))
 
@@ -608,13 +613,16 @@ def run_gpu(args, d: Dist) -> None:
     torch.cuda.synchronize()
     graph_ok = all(torch.equal(h_out[j].to(dev), dout[0]) for j in range(wl.nranks))
     replays = max(1, e2e_steps // per_graph)
-    with torch.cuda.stream(stream):          # replay() launches on the current stream
-        t_start.record(stream)
-        for _ in range(replays):
-            graph.replay()
-        t_end.record(stream)
-    t_end.synchronize()
-    graph_ms = d.max(t_start.elapsed_time(t_end)) / (replays * per_graph)
+    graph_ms = float("inf")
+    for _ in range(3):                       # best of three trials
+        with torch.cuda.stream(stream):      # replay() launches on the current stream
+            torch.cuda.synchronize()
+            t_start.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            t_end.record(stream)
+        t_end.synchronize()
+        graph_ms = min(graph_ms, d.max(t_start.elapsed_time(t_end)) / (replays * per_graph))
     del graph
 
     # Zero copy: the kernel reads the pinned host inputs and writes the pinned
@@ -631,9 +639,14 @@ def run_gpu(args, d: Dist) -> None:
         zero_copy_step()
         torch.cuda.synchronize()
         zc_ok = all(torch.equal(h_out[j].to(dev), dout[0]) for j in range(wl.nranks))
-        zc_ms = d.max(time_calls(torch, zero_copy_step, max(3, e2e_steps // 2), stream))
-    e2e_ms = min(eager_ms, graph_ms)
-    e2e_ok = e2e_ok and graph_ok
+        zc_ms = min(d.max(time_calls(torch, zero_copy_step, max(3, e2e_steps // 2), stream)) for _ in range(3))
+    # Three ways through the C ABI from pinned host buffers: pipelined copies
+    # issued eagerly or from a CUDA graph, or the kernel on the host buffers
+    # themselves.  Each moves every input in and every output out per step.
+    variants = {"pipelined_eager": eager_ms, "pipelined_cuda_graph": graph_ms, "zero_copy_kernel": zc_ms}
+    e2e_variant = min(variants, key=variants.get)
+    e2e_ms = variants[e2e_variant]
+    e2e_ok = e2e_ok and graph_ok and zc_ok
 
     # The platform's ceiling for that traffic: the same pinned copies alone
     # (H2D of all inputs, D2H of all outputs) and both directions at once.
@@ -744,9 +757,12 @@ def run_gpu(args, d: Dist) -> None:
                     "h2d_bytes_per_step": wl.nranks * wl.bytes_per_rank,
                     "d2h_bytes_per_step": wl.nranks * wl.bytes_per_rank, "steps": e2e_steps,
                     "ms_per_step": round(e2e_ms, 3), "outputs_identical": e2e_ok,
-                    "how": f"pinned host -> device copies, sar_allreduce, device -> pinned host copies of all "
-                           f"{wl.nranks} inputs and outputs every step, pipelined in {len(bounds)} chunks over "
-                           f"H2D / compute / D2H streams (faster of eager and CUDA-graph issue)",
+                    "how": f"all {wl.nranks} inputs from pinned host memory and all outputs back to it every "
+                           f"step through sar_allreduce, the fastest of three ways: pinned copies pipelined in "
+                           f"{len(bounds)} chunks over H2D / compute / D2H streams issued eagerly or from a CUDA "
+                           f"graph, or the kernel reading and writing the pinned host buffers itself "
+                           f"(best of three trials each); this run: {e2e_variant}",
+                    "variant": e2e_variant,
                     "copy_limits": copy_limits, "timing_note": timing_note,
                     "variants_ms_per_step": {"pipelined_eager": round(eager_ms, 3),
                                              "pipelined_cuda_graph": round(graph_ms, 3),
