@@ -88,6 +88,44 @@ sar_status check_rsag(const void* const* in, void* const* out, int nranks, size_
     return SAR_OK;
 }
 
+// Buffers that are not all 16-byte aligned but share one misalignment (every
+// address equal mod 16, as for slices at the same element offset of aligned
+// buffers): the first `head` elements, up to the 16-byte boundary, go to the
+// element kernels and the rest to the vector kernels on pointers advanced by
+// `head`.  Every element is reduced on its own, so the values are those of one
+// pass; the split only decides which kernel runs.  Returns 0 when it does not
+// apply.
+size_t common_head(const RankPtrs& p, int nranks, size_t count, size_t es) {
+    const uintptr_t m = reinterpret_cast<uintptr_t>(p.out[0]) & 15u;
+    if (m == 0 || m % es != 0) return 0;
+    for (int r = 0; r < nranks; ++r)
+        if ((reinterpret_cast<uintptr_t>(p.in[r]) & 15u) != m || (reinterpret_cast<uintptr_t>(p.out[r]) & 15u) != m)
+            return 0;
+    const size_t head = (16 - m) / es;
+    return head < count ? head : 0;
+}
+
+RankPtrs advance(const RankPtrs& p, int nranks, size_t bytes) {
+    RankPtrs q;
+    std::memset(&q, 0, sizeof(q));
+    for (int r = 0; r < nranks; ++r) {
+        q.in[r] = static_cast<const char*>(p.in[r]) + bytes;
+        q.out[r] = static_cast<char*>(p.out[r]) + bytes;
+    }
+    return q;
+}
+
+// Runs `launch(p, count, vec)` once, or twice (element-wise head, then the
+// vectors) when the buffers share a misalignment.
+template <class F>
+sar_status split_by_alignment(const RankPtrs& p, int nranks, size_t count, size_t es, bool vec, F&& launch) {
+    const size_t head = vec ? 0 : common_head(p, nranks, count, es);
+    if (head == 0) return launch(p, count, vec);
+    const sar_status st = launch(p, head, false);
+    if (st != SAR_OK) return st;
+    return launch(advance(p, nranks, head * es), count - head, true);
+}
+
 // Common checks of the LL entry points: rank count, element type, epoch,
 // packet buffers (16-byte aligned) and the buffers of one side (`data`: the
 // inputs of pack, the outputs of unpack-reduce).  *data16 tells whether every
@@ -171,12 +209,14 @@ SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nr
     bool vec = false, launch = false;
     sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
     if (st != SAR_OK || !launch) return st;
-    const size_t chunk = rsag_chunk(count, nranks, dtype);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (algo == SAR_ALGO_RSAG) return to_status(launch_rsag(kFused, dtype, nranks, p, count, chunk, vec, s));
-    st = to_status(launch_rsag(kReduceScatter, dtype, nranks, p, count, chunk, vec, s));
-    if (st != SAR_OK) return st;
-    return to_status(launch_all_gather(nranks, p, count, esize_of(dtype), chunk, vec, s));
+    return split_by_alignment(p, nranks, count, esize_of(dtype), vec, [&](const RankPtrs& q, size_t n, bool v) {
+        const size_t chunk = rsag_chunk(n, nranks, dtype);
+        if (algo == SAR_ALGO_RSAG) return to_status(launch_rsag(kFused, dtype, nranks, q, n, chunk, v, s));
+        const sar_status r = to_status(launch_rsag(kReduceScatter, dtype, nranks, q, n, chunk, v, s));
+        if (r != SAR_OK) return r;
+        return to_status(launch_all_gather(nranks, q, n, esize_of(dtype), chunk, v, s));
+    });
 }
 
 SAR_API sar_status sar_allreduce_accum(const void* const* in, void* const* out, int nranks, size_t count,
@@ -188,10 +228,12 @@ SAR_API sar_status sar_allreduce_accum(const void* const* in, void* const* out, 
     bool vec = false, launch = false;
     sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
     if (st != SAR_OK || !launch) return st;
-    const size_t chunk = rsag_chunk(count, nranks, dtype);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (accum == SAR_FP32) return to_status(launch_rsag(kFused, dtype, nranks, p, count, chunk, vec, s));
-    return to_status(launch_rsag_accum(dtype, accum, nranks, p, count, chunk, vec, s));
+    return split_by_alignment(p, nranks, count, esize_of(dtype), vec, [&](const RankPtrs& q, size_t n, bool v) {
+        const size_t chunk = rsag_chunk(n, nranks, dtype);
+        if (accum == SAR_FP32) return to_status(launch_rsag(kFused, dtype, nranks, q, n, chunk, v, s));
+        return to_status(launch_rsag_accum(dtype, accum, nranks, q, n, chunk, v, s));
+    });
 }
 
 SAR_API sar_status sar_reduce_scatter(const void* const* in, void* const* out, int nranks, size_t count,

@@ -39,8 +39,10 @@
  *    results.
  *  - Buffers must be aligned to their element size (else SAR_ERR_MISALIGNED).
  *    When every buffer of a call is 16-byte aligned the kernels move 16-byte
- *    vectors; otherwise a slower element-wise kernel runs.  Results are
- *    identical either way.
+ *    vectors.  sar_allreduce and sar_allreduce_accum also do when every buffer
+ *    has the same address modulo 16 (the elements up to the 16-byte boundary
+ *    run element-wise); otherwise a slower element-wise kernel runs.  Results
+ *    are identical either way.
  *  - A failed launch returns SAR_ERR_CUDA.
  *  - Kernels are launched with programmatic stream serialization (programmatic
  *    dependent launch): one may be scheduled while the work before it in the

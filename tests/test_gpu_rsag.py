@@ -214,6 +214,64 @@ def test_signed_zero_sums_any_rank_count(sar, dt, n):
         assert np.array_equal(gout[0].bytes(), want.view(np.uint8))
 
 
+
+@pytest.mark.parametrize("algo", [0, 1], ids=["rsag", "two_phase"])
+@pytest.mark.parametrize("n", [2, 5, 8])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_common_misalignment_splits_head_and_vectors(sar, dt, n, algo):
+    """Every buffer at the same element offset past a 16-byte boundary: the
+    head up to the boundary runs element-wise, the rest on 16-byte vectors;
+    the values equal the oracle's for every offset (and for counts that end
+    inside the head)."""
+    per16 = 16 // ESIZE[dt]
+    rng = np.random.default_rng([DTYPES.index(dt), n, algo, 3])
+    for k in sorted({1, per16 // 2, per16 - 1}):
+        for count in (1, per16 - k, per16 - k + 1, 4097 + k):
+            ins = [random_codes(rng, dt, count) for _ in range(n)]
+            want = oracle.allreduce(ins, dt)[0]
+            gin, gout = _run(sar, ins, dt, algo, offsets=[k * ESIZE[dt]] * n)
+            _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("dt,acc", [("e4m3fn", "e4m3fn"), ("bf16", "fp16"), ("e4m3b15", "fp16")])
+def test_common_misalignment_with_accumulator(sar, dt, acc):
+    rng = np.random.default_rng(17)
+    n, count, k = 4, 20011, 3
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce_accum(ins, dt, acc)[0]
+    gin = [Guarded.from_codes(c, k * ESIZE[dt]) for c in ins]
+    gout = [Guarded(count * ESIZE[dt], k * ESIZE[dt], fill=0x5A) for _ in range(n)]
+    sar.sar_allreduce_accum([g.ptr for g in gin], [g.ptr for g in gout], acc, count=count, dtype=dt)
+    torch.cuda.synchronize()
+    _check(gin, gout, ins, want, dt)
+
+
+def test_common_misalignment_runs_at_vector_speed(sar):
+    """At 2 x 64 MiB bf16, one element past the boundary on every buffer runs
+    within 10% of the aligned call (the element kernel alone is several
+    times slower)."""
+    count = 32 << 20
+    base_in = [torch.zeros(count + 8, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    base_out = [torch.empty(count + 8, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+
+    def ms(off):
+        pi = [t.data_ptr() + 2 * off for t in base_in]
+        po = [t.data_ptr() + 2 * off for t in base_out]
+        for _ in range(3):
+            sar.sar_allreduce(pi, po, count=count, dtype="bf16")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(10):
+            sar.sar_allreduce(pi, po, count=count, dtype="bf16")
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 10
+
+    aligned, shifted = min(ms(0) for _ in range(2)), min(ms(1) for _ in range(2))
+    assert shifted < 1.10 * aligned, (aligned, shifted)
+
+
 def test_rank_order_is_fixed(sar):
     """In binary32 ((2^24 + 1) - 2^24) + 1 = 1, while any other grouping or
     the reversed order gives 2."""
