@@ -12,12 +12,15 @@
 //                   binary32, rounds once and writes the elements to all N
 //                   outputs.
 //
-// Threads move 16 bytes of payload (4 packets, 32 bytes of packet buffer) at
-// a time with two 16-byte accesses; each 16-byte access is two
-// single-copy-atomic 8-byte packets.  Every poll is bounded: after max_spins
-// re-reads the thread records SAR_ERR_TIMEOUT in the caller's status word and
-// returns, and every other thread that has to wait returns as soon as it sees
-// a non-zero status.
+// A pack thread turns 16 bytes of input into 4 packets (32 bytes of packet
+// buffer): one 32-byte store when every packet buffer is 32-byte aligned, two
+// 16-byte stores otherwise.  An unpack thread takes one packet index: an
+// 8-byte load from each rank, all issued before the in-order adds.  A vector
+// access is a set of single-copy-atomic 8-byte element accesses, so a packet's
+// payload and flag are always written and read together.  Every poll is
+// bounded: after max_spins re-reads the thread records SAR_ERR_TIMEOUT in the
+// caller's status word and returns, and every other thread that has to wait
+// returns as soon as it sees a non-zero status.
 #include "sar_device.cuh"
 #include "sar_internal.h"
 
@@ -26,33 +29,26 @@ namespace {
 
 constexpr unsigned kMaxSleepNs = 1024;
 
+// Four packets in one 32-byte access (sm_100 and later); p must be 32-byte
+// aligned.  Each 8-byte element is still a single-copy-atomic access.
+__device__ __forceinline__ void st_packets4(uint64_t* p, uint64_t a, uint64_t b, uint64_t c, uint64_t d) {
+    asm volatile("st.volatile.global.v4.u64 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "l"(a), "l"(b), "l"(c), "l"(d) : "memory");
+}
+
+// One payload word of the result, not kept in L1.
+__device__ __forceinline__ void st_stream_word(uint32_t* p, uint32_t v) {
+    asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int32_t ld_status(const int32_t* s) {
     int32_t v;
     asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
     return v;
 }
 
-// Wait until four consecutive packets (already loaded into w) carry `epoch`.
-// Returns false when this thread gave up or saw another thread give up.
-__device__ __forceinline__ bool poll_quad(const uint64_t* src, uint32_t epoch, uint64_t max_spins, int32_t* status,
-                          uint64_t (&w)[4]) {
-    unsigned ns = 32;
-    for (uint64_t spin = 0;; ++spin) {
-        if (packet_flag(w[0]) == epoch && packet_flag(w[1]) == epoch && packet_flag(w[2]) == epoch &&
-            packet_flag(w[3]) == epoch)
-            return true;
-        if (spin >= max_spins) {
-            atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
-            return false;
-        }
-        if (ld_status(status) != 0) return false;
-        __nanosleep(ns);
-        if (ns < kMaxSleepNs) ns *= 2;
-        ld_packets2(src, w[0], w[1]);
-        ld_packets2(src + 2, w[2], w[3]);
-    }
-}
-
+// Wait until the packet (already loaded into w) carries `epoch`.  Returns
+// false when this thread gave up or saw another thread give up.
 __device__ __forceinline__ bool poll_one(const uint64_t* src, uint32_t epoch, uint64_t max_spins, int32_t* status,
                          uint64_t& w) {
     unsigned ns = 32;
@@ -70,29 +66,36 @@ __device__ __forceinline__ bool poll_one(const uint64_t* src, uint32_t epoch, ui
 }
 
 // ---------------------------------------------------------------------------
-// Pack.  p.in[r] = input, p.out[r] = packet buffer of rank r.
+// Pack.  p.in[r] = input, p.out[r] = packet buffer of rank r.  One 16-byte
+// input vector per thread; kWide: every packet buffer is 32-byte aligned.
 // ---------------------------------------------------------------------------
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads)
 ll_pack_vec_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
     pdl_wait();
     const int r = blockIdx.y;
-    const uint4* src = static_cast<const uint4*>(p.in[r]);
     uint64_t* dst = static_cast<uint64_t*>(p.out[r]);
     const size_t nq = nbytes / 16;
-    for (size_t q = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; q < nq;
-         q += static_cast<size_t>(gridDim.x) * kThreads) {
-        const uint4 x = ld_stream(src + q);
-        st_packets2(dst + 4 * q, make_packet(x.x, epoch), make_packet(x.y, epoch));
-        st_packets2(dst + 4 * q + 2, make_packet(x.z, epoch), make_packet(x.w, epoch));
+    const size_t q = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (q < nq) {
+        const uint4 x = ld_stream(static_cast<const uint4*>(p.in[r]) + q);
+        const uint64_t a = make_packet(x.x, epoch), b = make_packet(x.y, epoch);
+        const uint64_t c = make_packet(x.z, epoch), d = make_packet(x.w, epoch);
+        if (kWide) {
+            st_packets4(dst + 4 * q, a, b, c, d);
+        } else {
+            st_packets2(dst + 4 * q, a, b);
+            st_packets2(dst + 4 * q + 2, c, d);
+        }
     }
     // Up to 4 packets after the last whole 16 bytes; the last may be padded.
     if (blockIdx.x == 0 && threadIdx.x < 4) {
         const size_t w = 4 * nq + threadIdx.x;
         if (4 * w < nbytes) {
-            const unsigned char* b = static_cast<const unsigned char*>(p.in[r]);
+            const unsigned char* bytes = static_cast<const unsigned char*>(p.in[r]);
             uint32_t payload = 0;
             for (int k = 0; k < 4; ++k)
-                if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
+                if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(bytes[4 * w + k]) << (8 * k);
             st_packet(dst + w, make_packet(payload, epoch));
         }
     }
@@ -117,84 +120,53 @@ ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
 
 // ---------------------------------------------------------------------------
 // Poll + unpack + reduce + write-back.  p.in[k] = packet buffer of rank k,
-// p.out[j] = output of rank j.  Rank r (blockIdx.y) owns packet groups
-// [r*chunk_q, min(nq, (r+1)*chunk_q)), a group being 4 packets = 16 payload
-// bytes.
+// p.out[j] = output of rank j.  Rank r (blockIdx.y) owns packets
+// [r*chunk, min(npk, (r+1)*chunk)), one packet index per thread; vec_out:
+// every output is 16-byte aligned, so whole payload words are stored.
 // ---------------------------------------------------------------------------
 template <int DT, int NR>
 __global__ void __launch_bounds__(kThreads)
-ll_unpack_reduce_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t epoch,
+ll_unpack_reduce_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk, uint32_t epoch,
                         uint64_t max_spins, int32_t* status, bool vec_out) {
     pdl_wait();
-    constexpr int VE = Elem<DT>::kVE;
     constexpr int EP = PerWord<DT>::kN;
     constexpr int WIN = NR == 0 ? 4 : (NR < 8 ? NR : 8);
     const int n = ranks<NR>(n_rt);
-    const int r = blockIdx.y;
     const size_t npk = (nbytes + 3) / 4;
-    const size_t nq = (npk + 3) / 4;
-    const size_t qb = static_cast<size_t>(r) * chunk_q;
-    if (qb >= nq) return;
-    const size_t qe = min(nq, qb + chunk_q);
-
-    for (size_t q = qb + static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; q < qe;
-         q += static_cast<size_t>(gridDim.x) * kThreads) {
-        if (16 * (q + 1) <= nbytes) {
-            // A whole group: 4 packets of payload from every rank.
-            Acc<DT> acc;
-// Windows of 8 ranks run as a loop (one window for up to 8 ranks).
+    const size_t wb = static_cast<size_t>(blockIdx.y) * chunk;
+    const size_t w = wb + static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (w >= min(npk, wb + chunk)) return;
+    float acc[EP];
+// Windows of up to 8 ranks: every load of a window is issued before its adds.
 #pragma unroll 1
-            for (int k0 = 0; k0 < n; k0 += WIN) {
-                uint64_t w[WIN][4];
+    for (int k0 = 0; k0 < n; k0 += WIN) {
+        uint64_t pk[WIN];
 #pragma unroll
-                for (int k = 0; k < WIN; ++k) {
-                    if (NR == 0 && k0 + k >= n) break;
-                    const uint64_t* src = static_cast<const uint64_t*>(p.in[k0 + k]) + 4 * q;
-                    ld_packets2(src, w[k][0], w[k][1]);
-                    ld_packets2(src + 2, w[k][2], w[k][3]);
-                }
+        for (int k = 0; k < WIN; ++k) {
+            if (NR == 0 && k0 + k >= n) break;
+            pk[k] = ld_packet(static_cast<const uint64_t*>(p.in[k0 + k]) + w);
+        }
 #pragma unroll
-                for (int k = 0; k < WIN; ++k) {
-                    if (NR == 0 && k0 + k >= n) break;
-                    const uint64_t* src = static_cast<const uint64_t*>(p.in[k0 + k]) + 4 * q;
-                    if (!poll_quad(src, epoch, max_spins, status, w[k])) return;
-                    const uint4 x = make_uint4(packet_payload(w[k][0]), packet_payload(w[k][1]),
-                                               packet_payload(w[k][2]), packet_payload(w[k][3]));
-                    if (k0 + k == 0) acc_seed<DT>(acc, x);
-                    else acc_add<DT>(acc, x);
-                }
-            }
-            if (vec_out) {
-                const uint4 y = acc_round<DT>(acc);
+        for (int k = 0; k < WIN; ++k) {
+            if (NR == 0 && k0 + k >= n) break;
+            if (!poll_one(static_cast<const uint64_t*>(p.in[k0 + k]) + w, epoch, max_spins, status, pk[k])) return;
+            float x[EP];
+            widen_word<DT>(packet_payload(pk[k]), x);
 #pragma unroll
-                for (int j = 0; j < n; ++j) st_stream(static_cast<uint4*>(p.out[j]) + q, y);
-            } else {
+            for (int e = 0; e < EP; ++e) acc[e] = (k0 + k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
+        }
+    }
+    if (vec_out && 4 * (w + 1) <= nbytes) {
+        const uint32_t y = narrow_word<DT>(acc);
 #pragma unroll
-                for (int e = 0; e < VE; ++e)
+        for (int j = 0; j < n; ++j) st_stream_word(static_cast<uint32_t*>(p.out[j]) + w, y);
+    } else {
+        // Unaligned outputs, or the last payload word holding fewer elements.
 #pragma unroll
-                    for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], q * VE + e, acc.v[e]);
-            }
-        } else {
-            // The last group: 1..4 packets, the last one possibly padded.
-            const size_t wend = min(npk, 4 * q + 4);
-            for (size_t w = 4 * q; w < wend; ++w) {
-                float acc[EP];
-                for (int k = 0; k < n; ++k) {
-                    const uint64_t* src = static_cast<const uint64_t*>(p.in[k]) + w;
-                    uint64_t pk = ld_packet(src);
-                    if (!poll_one(src, epoch, max_spins, status, pk)) return;
-                    float x[EP];
-                    widen_word<DT>(packet_payload(pk), x);
-#pragma unroll
-                    for (int e = 0; e < EP; ++e) acc[e] = (k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
-                }
-#pragma unroll
-                for (int e = 0; e < EP; ++e) {
-                    const size_t i = w * EP + e;
-                    if (i < count)
-                        for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], i, acc[e]);
-                }
-            }
+        for (int e = 0; e < EP; ++e) {
+            const size_t i = w * EP + e;
+            if (i < count)
+                for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], i, acc[e]);
         }
     }
 }
@@ -206,16 +178,20 @@ inline unsigned grid_x(size_t items, size_t cap) {
     return static_cast<unsigned>(g);
 }
 
+// The byte-wise pack loops over its packets; the vector kernels take one
+// item per thread, and a grid they cannot cover is refused.
 constexpr size_t kGridCap = 65535;
+constexpr size_t kMaxGridX = 0x7FFFFFFF;
 
 template <int DT, int NR>
 cudaError_t unpack_dispatch(int nranks, const RankPtrs& p, size_t count, uint32_t epoch, uint64_t max_spins,
                             int32_t* status, bool vec_out, cudaStream_t s) {
     const size_t nbytes = count * Elem<DT>::kSize;
-    const size_t npk = (nbytes + 3) / 4, nq = (npk + 3) / 4;
-    const size_t chunk_q = (nq + nranks - 1) / nranks;
-    const dim3 grid(grid_x(chunk_q, kGridCap), nranks);
-    launch_kernel(ll_unpack_reduce_kernel<DT, NR>, grid, dim3(kThreads), s, p, nranks, count, nbytes, chunk_q,
+    const size_t npk = (nbytes + 3) / 4;
+    const size_t chunk = (npk + nranks - 1) / nranks;
+    if ((chunk + kThreads - 1) / kThreads > kMaxGridX) return cudaErrorInvalidValue;
+    const dim3 grid(grid_x(chunk, kMaxGridX), nranks);
+    launch_kernel(ll_unpack_reduce_kernel<DT, NR>, grid, dim3(kThreads), s, p, nranks, count, nbytes, chunk,
                   epoch, max_spins, status, vec_out);
     return cudaGetLastError();
 }
@@ -241,8 +217,12 @@ cudaError_t unpack_ranks(int nranks, const RankPtrs& p, size_t count, uint32_t e
 cudaError_t launch_ll_pack(int nranks, const RankPtrs& p, size_t bytes, uint32_t epoch, bool vec,
                            cudaStream_t stream) {
     if (vec) {
-        const dim3 grid(grid_x(bytes / 16 + 1, kGridCap), nranks);
-        launch_kernel(ll_pack_vec_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);
+        if ((bytes / 16 + kThreads) / kThreads > kMaxGridX) return cudaErrorInvalidValue;
+        const dim3 grid(grid_x(bytes / 16 + 1, kMaxGridX), nranks);
+        bool wide = true;
+        for (int r = 0; r < nranks; ++r) wide = wide && reinterpret_cast<uintptr_t>(p.out[r]) % 32 == 0;
+        if (wide) launch_kernel(ll_pack_vec_kernel<true>, grid, dim3(kThreads), stream, p, bytes, epoch);
+        else launch_kernel(ll_pack_vec_kernel<false>, grid, dim3(kThreads), stream, p, bytes, epoch);
     } else {
         const dim3 grid(grid_x((bytes + 3) / 4, kGridCap), nranks);
         launch_kernel(ll_pack_bytes_kernel, grid, dim3(kThreads), stream, p, bytes, epoch);

@@ -57,6 +57,37 @@ def test_pack_unpack_match_oracle(sar, dt, n, count):
         assert_same(g.codes(dt), ins[r], dt, "input modified")
 
 
+@pytest.mark.parametrize("which", ["rank0", "all"])
+@pytest.mark.parametrize("count", [1, 7, 1031, 65541])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_pack_into_16_but_not_32_byte_aligned_packets(sar, dt, count, which):
+    """Packet buffers at 16 mod 32 (one rank, or all) take the two-16-byte-store
+    pack instead of the 32-byte one; the packet image and the sums are the same."""
+    n = 4
+    rng = np.random.default_rng([DTYPES.index(dt), count, 16])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    epoch = 0x0A0B0C0D
+    gin = [Guarded.from_codes(c) for c in ins]
+    offs = [16 if (which == "all" or r == 0) else 0 for r in range(n)]
+    pk = [Guarded(sar.sar_ll_packet_bytes(count, dt), o, fill=0) for o in offs]
+    assert pk[0].ptr % 32 == 16
+    sar.sar_ll_pack([g.ptr for g in gin], [g.ptr for g in pk], epoch, count=count, dtype=dt)
+    torch.cuda.synchronize()
+    want_pk = oracle.ll_pack(ins, dt, epoch)
+    for r in range(n):
+        assert np.array_equal(pk[r].bytes(), want_pk[r]), f"packet image of rank {r}"
+        assert pk[r].guards_intact()
+    st = _status()
+    gout = [Guarded(count * ESIZE[dt]) for _ in range(n)]
+    sar.sar_allreduce_ll([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], epoch + 1, st,
+                         count=count, dtype=dt)
+    assert sar.sar_read_device_status(st) == sar.SAR_OK
+    want = oracle.allreduce(ins, dt)[0]
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+        assert g.guards_intact()
+
+
 @pytest.mark.parametrize("dt", DTYPES)
 def test_unpack_reads_oracle_packets(sar, dt):
     """Packets written by the oracle (not by the GPU) unpack to the oracle's sums."""
