@@ -21,6 +21,7 @@
 // bounded: after max_spins re-reads the thread records SAR_ERR_TIMEOUT in the
 // caller's status word and returns, and every other thread that has to wait
 // returns as soon as it sees a non-zero status.
+#include "ll_packets.cuh"
 #include "sar_device.cuh"
 #include "sar_internal.h"
 
@@ -28,18 +29,6 @@ namespace sar {
 namespace {
 
 constexpr unsigned kMaxSleepNs = 1024;
-
-// Four packets in one 32-byte access (sm_100 and later); p must be 32-byte
-// aligned.  Each 8-byte element is still a single-copy-atomic access.
-__device__ __forceinline__ void st_packets4(uint64_t* p, uint64_t a, uint64_t b, uint64_t c, uint64_t d) {
-    asm volatile("st.volatile.global.v4.u64 [%0], {%1, %2, %3, %4};"
-                 :: "l"(p), "l"(a), "l"(b), "l"(c), "l"(d) : "memory");
-}
-
-// One payload word of the result, not kept in L1.
-__device__ __forceinline__ void st_stream_word(uint32_t* p, uint32_t v) {
-    asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ int32_t ld_status(const int32_t* s) {
     int32_t v;

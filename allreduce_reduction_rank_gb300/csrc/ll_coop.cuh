@@ -4,10 +4,12 @@
 //
 // mscclpp commit history, the allreduce_allpair_packet fix: the same thread
 // block sends, reduces and writes back.  Every block of simulated rank r
-//   A. packs its share of rank r's input into pkts[r] (the send);
+//   A. packs its share of rank r's input into pkts[r] (the send): 16 input
+//      bytes per thread and step, as one 32-byte packet store when every
+//      packet buffer is 32-byte aligned, else two 16-byte stores;
 //   B. polls its share of rank r's packet chunk in all N packet buffers (the
-//      packets are written by other blocks of the same launch), reduces in
-//      rank order and rounds once;
+//      packets are written by other blocks of the same launch), one packet
+//      index per thread and step, reduces in rank order and rounds once;
 //   C. writes the result back, in one of three ways (template WB):
 //        kDirect     - plain stores from registers to all N outputs;
 //        kPacketsAll - as flagged result packets into `res`; then a block of
@@ -16,7 +18,10 @@
 //                      read-once, write-to-several-destinations fusion of the
 //                      commit history's ReadPutPacket change);
 //        kPacketsOwn - as result packets; then every rank j polls all result
-//                      packets and writes its own output only.
+//                      packets, starting with its own chunk, and writes its
+//                      own output only.
+//      Result packets are read 4 at a time (16-byte loads); rank chunks are
+//      whole groups of 4 packets, so a group never spans two chunks.
 // Each 8-byte packet is one single-copy-atomic store and load, so a flag that
 // matches the epoch guarantees its payload; a stale flag means "not arrived".
 // Every poll is bounded.  Blocks wait on one another, so the launch is
@@ -31,6 +36,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "ll_packets.cuh"
 #include "sar_device.cuh"
 #include "sar_internal.h"
 
@@ -101,8 +107,8 @@ template <int DT> __device__ __forceinline__ void store_bits(void* base, size_t 
 }
 
 // Phase A: rank r's input -> pkts[r].
-__device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t epoch, bool in16, size_t tid,
-                                     size_t stride) {
+__device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t epoch, bool in16, bool pk32,
+                                     size_t tid, size_t stride) {
     const int r = blockIdx.y;
     const size_t npk = (nbytes + 3) / 4;
     uint64_t* mine = a.pkts[r];
@@ -111,8 +117,14 @@ __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t ep
         const uint4* src = static_cast<const uint4*>(a.data.in[r]);
         for (size_t q = tid; q < nfull; q += stride) {
             const uint4 x = ld_stream(src + q);
-            st_packets2(mine + 4 * q, make_packet(x.x, epoch), make_packet(x.y, epoch));
-            st_packets2(mine + 4 * q + 2, make_packet(x.z, epoch), make_packet(x.w, epoch));
+            const uint64_t p0 = make_packet(x.x, epoch), p1 = make_packet(x.y, epoch);
+            const uint64_t p2 = make_packet(x.z, epoch), p3 = make_packet(x.w, epoch);
+            if (pk32) {
+                st_packets4(mine + 4 * q, p0, p1, p2, p3);
+            } else {
+                st_packets2(mine + 4 * q, p0, p1);
+                st_packets2(mine + 4 * q + 2, p2, p3);
+            }
         }
     }
     const unsigned char* b = static_cast<const unsigned char*>(a.data.in[r]);
@@ -124,98 +136,73 @@ __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t ep
     }
 }
 
-// Phase B (+ C for kDirect): reduce rank r's chunk.  False when a poll gave up.
+// Phase B (+ C for kDirect): reduce rank r's chunk of packets
+// [r*chunk, (r+1)*chunk), one packet index per thread and iteration.  False
+// when a poll gave up.
 template <int DT, int NR, int WB>
-__device__ __forceinline__ bool reduce(const LLArgs& a, int n_rt, size_t count, size_t nbytes, size_t chunk_q,
+__device__ __forceinline__ bool reduce(const LLArgs& a, int n_rt, size_t count, size_t nbytes, size_t chunk,
                                        uint32_t epoch, uint64_t max_spins, int32_t* status, bool out16, size_t tid,
                                        size_t stride) {
-    constexpr int VE = Elem<DT>::kVE;
     constexpr int EP = PerWord<DT>::kN;
     constexpr int WIN = NR == 0 ? 4 : (NR < 8 ? NR : 8);
     const int n = ranks<NR>(n_rt);
-    const int r = blockIdx.y;
     const size_t npk = (nbytes + 3) / 4;
-    const size_t nq = (npk + 3) / 4;
-    const size_t qb = static_cast<size_t>(r) * chunk_q;
-    const size_t qe = min(nq, qb + chunk_q);
-    for (size_t q = qb + tid; q < qe; q += stride) {
-        if (16 * (q + 1) <= nbytes) {
-            Acc<DT> acc;
+    const size_t wb = static_cast<size_t>(blockIdx.y) * chunk;
+    const size_t we = min(npk, wb + chunk);
+    for (size_t w = wb + tid; w < we; w += stride) {
+        float acc[EP];
 #pragma unroll 1
-            for (int k0 = 0; k0 < n; k0 += WIN) {
-                uint64_t w[WIN][4];
+        for (int k0 = 0; k0 < n; k0 += WIN) {
+            uint64_t pk[WIN][1];
 #pragma unroll
-                for (int k = 0; k < WIN; ++k) {
-                    if (NR == 0 && k0 + k >= n) break;
-                    const uint64_t* src = a.pkts[k0 + k] + 4 * q;
-                    ld_packets2(src, w[k][0], w[k][1]);
-                    ld_packets2(src + 2, w[k][2], w[k][3]);
-                }
-#pragma unroll
-                for (int k = 0; k < WIN; ++k) {
-                    if (NR == 0 && k0 + k >= n) break;
-                    if (!poll<4>(a.pkts[k0 + k] + 4 * q, epoch, max_spins, status, w[k])) return false;
-                    const uint4 x = make_uint4(packet_payload(w[k][0]), packet_payload(w[k][1]),
-                                               packet_payload(w[k][2]), packet_payload(w[k][3]));
-                    if (k0 + k == 0) acc_seed<DT>(acc, x);
-                    else acc_add<DT>(acc, x);
-                }
+            for (int k = 0; k < WIN; ++k) {
+                if (NR == 0 && k0 + k >= n) break;
+                pk[k][0] = ld_packet(a.pkts[k0 + k] + w);
             }
-            const uint4 y = acc_round<DT>(acc);
-            if constexpr (WB != kDirect) {
-                st_packets2(a.res + 4 * q, make_packet(y.x, epoch), make_packet(y.y, epoch));
-                st_packets2(a.res + 4 * q + 2, make_packet(y.z, epoch), make_packet(y.w, epoch));
-            } else if (out16) {
 #pragma unroll
-                for (int j = 0; j < n; ++j) st_stream(static_cast<uint4*>(a.data.out[j]) + q, y);
-            } else {
+            for (int k = 0; k < WIN; ++k) {
+                if (NR == 0 && k0 + k >= n) break;
+                if (!poll<1>(a.pkts[k0 + k] + w, epoch, max_spins, status, pk[k])) return false;
+                float x[EP];
+                widen_word<DT>(packet_payload(pk[k][0]), x);
 #pragma unroll
-                for (int e = 0; e < VE; ++e)
-#pragma unroll
-                    for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], q * VE + e, acc.v[e]);
+                for (int e = 0; e < EP; ++e) acc[e] = (k0 + k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
             }
+        }
+        if constexpr (WB != kDirect) {
+            // Elements past the end are zero bits, as in the send's padding.
+            float xs[EP];
+#pragma unroll
+            for (int e = 0; e < EP; ++e) xs[e] = (w * EP + e < count) ? acc[e] : 0.0f;
+            st_packet(a.res + w, make_packet(narrow_word<DT>(xs), epoch));
+        } else if (out16 && 4 * (w + 1) <= nbytes) {
+            const uint32_t y = narrow_word<DT>(acc);
+#pragma unroll
+            for (int j = 0; j < n; ++j) st_stream_word(static_cast<uint32_t*>(a.data.out[j]) + w, y);
         } else {
-            // The last group: 1..4 packets, the last one possibly padded.
-            const size_t wend = min(npk, 4 * q + 4);
-            for (size_t w = 4 * q; w < wend; ++w) {
-                float acc[EP];
-                for (int k = 0; k < n; ++k) {
-                    uint64_t pk[1] = {ld_packet(a.pkts[k] + w)};
-                    if (!poll<1>(a.pkts[k] + w, epoch, max_spins, status, pk)) return false;
-                    float x[EP];
-                    widen_word<DT>(packet_payload(pk[0]), x);
 #pragma unroll
-                    for (int e = 0; e < EP; ++e) acc[e] = (k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
-                }
-                if constexpr (WB != kDirect) {
-                    // Elements past the end are zero bits, as in the send's padding.
-                    float xs[EP];
-#pragma unroll
-                    for (int e = 0; e < EP; ++e) xs[e] = (w * EP + e < count) ? acc[e] : 0.0f;
-                    st_packet(a.res + w, make_packet(narrow_word<DT>(xs), epoch));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EP; ++e) {
-                        const size_t i = w * EP + e;
-                        if (i < count)
-                            for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], i, acc[e]);
-                    }
-                }
+            for (int e = 0; e < EP; ++e) {
+                const size_t i = w * EP + e;
+                if (i < count)
+                    for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], i, acc[e]);
             }
         }
     }
     return true;
 }
 
-// Phase C for the packet write-backs: poll result packets of groups
-// [qb, qe) (step `stride`) and store their payload to outputs [j0, j1).
+// Phase C for the packet write-backs: poll the result packets [wb, we) (wb a
+// multiple of 4), 4 at a time (step `stride` groups), and store their payload
+// to outputs [j0, j1).
 template <int DT>
-__device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, size_t nbytes, size_t qb, size_t qe,
-                                               int j0, int j1, uint32_t epoch, uint64_t max_spins, int32_t* status,
-                                               bool out16, size_t tid, size_t stride) {
+__device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, size_t nbytes, size_t wb, size_t we,
+                                               size_t rot, int j0, int j1, uint32_t epoch, uint64_t max_spins,
+                                               int32_t* status, bool out16, size_t tid, size_t stride) {
     constexpr int EP = PerWord<DT>::kN;
-    const size_t npk = (nbytes + 3) / 4;
-    for (size_t q = qb + tid; q < qe; q += stride) {
+    const size_t g0 = wb / 4, ng = (we + 3) / 4 - g0;
+    for (size_t i = tid; i < ng; i += stride) {
+        size_t q = g0 + i + rot;
+        if (q >= g0 + ng) q -= ng;
         if (16 * (q + 1) <= nbytes) {
             uint64_t w[4];
             ld_packets2(a.res + 4 * q, w[0], w[1]);
@@ -234,7 +221,7 @@ __device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, si
                         for (int e = 0; e < EP; ++e) store_bits<DT>(a.data.out[j], (4 * q + m) * EP + e, words[m], e);
             }
         } else {
-            const size_t wend = min(npk, 4 * q + 4);
+            const size_t wend = min(we, 4 * q + 4);
             for (size_t wi = 4 * q; wi < wend; ++wi) {
                 uint64_t pk[1] = {ld_packet(a.res + wi)};
                 if (!poll<1>(a.res + wi, epoch, max_spins, status, pk)) return false;
@@ -251,8 +238,8 @@ __device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, si
 
 template <int DT, int NR, int WB>
 __global__ void __launch_bounds__(kThreads)
-coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk_q, uint32_t host_epoch,
-            uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16) {
+coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk, uint32_t host_epoch,
+            uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
     pdl_wait();
     __shared__ uint32_t s_epoch;
     if (threadIdx.x == 0) {
@@ -268,21 +255,24 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk_
     const size_t tid = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
     const int n = ranks<NR>(n_rt);
-    send(a, nbytes, epoch, in16, tid, stride);
-    bool ok = reduce<DT, NR, WB>(a, n_rt, count, nbytes, chunk_q, epoch, max_spins, status, out16, tid, stride);
+    send(a, nbytes, epoch, in16, pk32, tid, stride);
+    bool ok = reduce<DT, NR, WB>(a, n_rt, count, nbytes, chunk, epoch, max_spins, status, out16, tid, stride);
+    const size_t npk = (nbytes + 3) / 4;
     if constexpr (WB == kPacketsAll) {
         // Chunk (r + 1) mod N, reduced by other blocks: each result packet is
         // read once and written to every output.
-        const size_t nq = ((nbytes + 3) / 4 + 3) / 4;
         const size_t c = (static_cast<size_t>(blockIdx.y) + 1) % n;
-        const size_t qb = c * chunk_q, qe = min(nq, qb + chunk_q);
-        if (ok && qb < qe)
-            unpack_results<DT>(a, count, nbytes, qb, qe, 0, n, epoch, max_spins, status, out16, tid, stride);
+        const size_t wb = c * chunk, we = min(npk, wb + chunk);
+        if (ok && wb < we)
+            unpack_results<DT>(a, count, nbytes, wb, we, 0, 0, n, epoch, max_spins, status, out16, tid, stride);
     } else if constexpr (WB == kPacketsOwn) {
-        // Rank j reads every result packet and writes its own output.
-        const size_t nq = ((nbytes + 3) / 4 + 3) / 4;
+        // Rank j reads every result packet and writes its own output, starting
+        // with its own chunk (reduced by this rank's blocks just before).
         const int j = blockIdx.y;
-        if (ok) unpack_results<DT>(a, count, nbytes, 0, nq, j, j + 1, epoch, max_spins, status, out16, tid, stride);
+        const size_t ng = (npk + 3) / 4, rot = min(ng, j * chunk / 4);
+        if (ok)
+            unpack_results<DT>(a, count, nbytes, 0, npk, rot == ng ? 0 : rot, j, j + 1, epoch, max_spins, status,
+                               out16, tid, stride);
     }
     if (ctrl != nullptr) {
         // Every block read ctrl[0] before arriving; the last block to arrive
@@ -306,8 +296,9 @@ template <int DT, int NR, int WB>
 cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint32_t* ctrl,
                           uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
     const size_t nbytes = count * Elem<DT>::kSize;
-    const size_t npk = (nbytes + 3) / 4, nq = (npk + 3) / 4;
-    const size_t chunk_q = (nq + nranks - 1) / nranks;
+    const size_t npk = (nbytes + 3) / 4;
+    // Packets per rank, a multiple of 4 so that result groups never straddle two chunks.
+    const size_t chunk = ((npk + nranks - 1) / nranks + 3) / 4 * 4;
     // Blocks per rank: enough threads for the largest phase, capped so that
     // all nranks * gx blocks are co-resident (resident blocks per SM x SMs,
     // looked up once per device).
@@ -327,14 +318,16 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
         blocks = sms * per_sm;
         resident[dev].store(blocks, std::memory_order_relaxed);
     }
-    size_t want = std::max<size_t>(div_up(npk, kThreads), div_up(chunk_q, kThreads));
-    if (WB == kPacketsOwn) want = std::max<size_t>(want, div_up(nq, kThreads));
+    size_t want = std::max<size_t>(div_up(in16 ? nbytes / 16 + 4 : npk, kThreads), div_up(chunk, kThreads));
+    if (WB == kPacketsOwn) want = std::max<size_t>(want, div_up((npk + 3) / 4, kThreads));
     const size_t cap = static_cast<size_t>(blocks) / nranks;
     if (cap == 0) return cudaErrorCooperativeLaunchTooLarge;
     const unsigned gx = static_cast<unsigned>(std::max<size_t>(1, std::min(want, cap)));
     LLArgs args = a;
     int n_rt = nranks;
-    size_t cnt = count, nb = nbytes, cq = chunk_q;
+    size_t cnt = count, nb = nbytes, cq = chunk;
+    bool p32 = true;
+    for (int r = 0; r < nranks; ++r) p32 = p32 && reinterpret_cast<uintptr_t>(a.pkts[r]) % 32 == 0;
     uint32_t ep = epoch;
     uint32_t* ct = ctrl;
     uint64_t ms = max_spins;
@@ -355,7 +348,8 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, coop_kernel<DT, NR, WB>, args, n_rt, cnt, nb, cq, ep, ct, ms, st, i16, o16);
+    return cudaLaunchKernelEx(&cfg, coop_kernel<DT, NR, WB>, args, n_rt, cnt, nb, cq, ep, ct, ms, st, i16, o16,
+                              p32);
 }
 
 template <int DT, int WB>

@@ -341,28 +341,4 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
-// LL packets: two 8-byte packets per 16-byte access.  A vector access is two
-// single-copy-atomic 8-byte accesses, so each packet's payload and flag are
-// always observed together.  volatile keeps every poll a fresh read.
-__device__ __forceinline__ void ld_packets2(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_packet(const uint64_t* p) {
-    uint64_t a;
-    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
-    return a;
-}
-__device__ __forceinline__ void st_packets2(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" :: "l"(p), "l"(a), "l"(b) : "memory");
-}
-__device__ __forceinline__ void st_packet(uint64_t* p, uint64_t a) {
-    asm volatile("st.volatile.global.u64 [%0], %1;" :: "l"(p), "l"(a) : "memory");
-}
-
-__device__ __forceinline__ uint64_t make_packet(uint32_t payload, uint32_t epoch) {
-    return static_cast<uint64_t>(payload) | (static_cast<uint64_t>(epoch) << 32);
-}
-__device__ __forceinline__ uint32_t packet_flag(uint64_t p) { return static_cast<uint32_t>(p >> 32); }
-__device__ __forceinline__ uint32_t packet_payload(uint64_t p) { return static_cast<uint32_t>(p); }
-
 }  // namespace sar

@@ -49,6 +49,30 @@ def test_fused_matches_oracle(sar, dt, n, count):
         assert pk[r].guards_intact()
 
 
+@pytest.mark.parametrize("count", [7, 4099, 65541])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_fused_packets_16_but_not_32_byte_aligned(sar, dt, count):
+    """Packet buffers at 16 mod 32 take the two-16-byte-store send."""
+    n = 4
+    rng = np.random.default_rng([DTYPES.index(dt), count, 32])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin = [Guarded.from_codes(c) for c in ins]
+    gout = [Guarded(count * ESIZE[dt]) for _ in range(n)]
+    pk = [Guarded(sar.sar_ll_packet_bytes(count, dt), 16 if r % 2 else 0, fill=0) for r in range(n)]
+    assert pk[1].ptr % 32 == 16
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sar.sar_allreduce_ll_fused([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], st, epoch=5,
+                               count=count, dtype=dt)
+    assert sar.sar_read_device_status(st) == sar.SAR_OK
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+    want_pk = oracle.ll_pack(ins, dt, 5)
+    for r in range(n):
+        assert np.array_equal(pk[r].bytes(), want_pk[r])
+        assert pk[r].guards_intact()
+
+
 @pytest.mark.parametrize("dt", DTYPES)
 def test_fused_unaligned(sar, dt):
     rng = np.random.default_rng(7)

@@ -22,13 +22,13 @@ def sar():
     return s
 
 
-def _run(sar, ins, dt, multi, epoch=None, ctrl=None, offsets=None):
+def _run(sar, ins, dt, multi, epoch=None, ctrl=None, offsets=None, pk_offset=0):
     n, count = len(ins), ins[0].size
     offs = offsets or [0] * n
     gin = [Guarded.from_codes(c, o) for c, o in zip(ins, offs)]
     gout = [Guarded(count * ESIZE[dt], o, fill=0x5A) for o in offs]
     nbp = sar.sar_ll_packet_bytes(count, dt)
-    pk = [Guarded(nbp, 0, fill=0) for _ in range(n)]
+    pk = [Guarded(nbp, pk_offset, fill=0) for _ in range(n)]
     res = Guarded(nbp, 0, fill=0)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     sar.sar_allreduce_ll_writeback([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], res.ptr, st,
@@ -61,6 +61,23 @@ def test_writeback_matches_oracle(sar, dt, n, count, multi):
     assert_same(payload.view(want.dtype), want, dt, "result packets")
     assert np.all(np.ascontiguousarray(got_res[:, :4]).ravel()[count * ESIZE[dt]:] == 0)   # zero padding
     assert res.guards_intact()
+
+
+@pytest.mark.parametrize("multi", [True, False], ids=["multi_dest", "own_output"])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_writeback_packets_16_but_not_32_byte_aligned(sar, dt, multi):
+    """Send packet buffers at 16 mod 32 take the two-16-byte-store send."""
+    rng = np.random.default_rng([DTYPES.index(dt), int(multi), 32])
+    ins = [random_codes(rng, dt, 4099) for _ in range(5)]
+    want = oracle.allreduce(ins, dt)[0]
+    _, gout, pk, _ = _run(sar, ins, dt, multi, epoch=11, pk_offset=16)
+    assert pk[0].ptr % 32 == 16
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+    want_pk = oracle.ll_pack(ins, dt, 11)
+    for r in range(5):
+        assert np.array_equal(pk[r].bytes(), want_pk[r])
+        assert pk[r].guards_intact()
 
 
 @pytest.mark.parametrize("multi", [True, False])
