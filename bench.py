@@ -228,6 +228,16 @@ def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, gr
     return row
 
 
+def rsag_result(torch, sar, din, wl, stream):
+    """The fused rsag allreduce of `din` (bit-exact against the oracle in the
+    GPU tests): the value every LL row's outputs must equal."""
+    outs = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    sar.sar_allreduce([t.data_ptr() for t in din], [t.data_ptr() for t in outs], count=wl.count, dtype=wl.dtype,
+                      stream=stream.cuda_stream)
+    stream.synchronize()
+    return outs[0]
+
+
 def ll_row(torch, sar, wl, dev, stream, calls):
     ins = wl.inputs()
     din = [upload(torch, x, wl.dtype, dev) for x in ins]
@@ -249,12 +259,14 @@ def ll_row(torch, sar, wl, dev, stream, calls):
         # a replay re-packs every packet before it is polled, so replays are safe.
         g_ms = time_graph(torch, call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    want = rsag_result(torch, sar, din, wl, stream)
+    same = all(torch.equal(t, want) for t in dout)
     phys = 6 * wl.nranks * wl.bytes_per_rank
     return {"workload": wl.name, "calls": calls, "epochs": f"1..{calls}", "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
             "physical_GBps": round(phys / (ms * 1e-3) / GB, 2),
             "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
-            "status_ok": ok}
+            "status_ok": ok, "outputs_ok": same}
 
 
 def ll_double_row(torch, sar, wl, dev, calls):
@@ -307,10 +319,11 @@ def ll_double_row(torch, sar, wl, dev, calls):
     g_ms = start.elapsed_time(end) / (2 * calls)
     del graph
     ok = all(sar.sar_read_device_status(x.data_ptr(), streams[0].cuda_stream) == sar.SAR_OK for x in st)
-    same = all(torch.equal(dout[s][j], dout[0][0]) for s in range(2) for j in range(wl.nranks))
+    want = rsag_result(torch, sar, din, wl, streams[0])
+    same = all(torch.equal(dout[s][j], want) for s in range(2) for j in range(wl.nranks))
     return {"workload": wl.name + "_double_two_streams", "calls": 2 * calls, "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2), "graph_us_per_call": round(g_ms * 1e3, 3),
-            "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2), "status_ok": ok and same}
+            "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2), "status_ok": ok, "outputs_ok": same}
 
 
 def ll_fused_row(torch, sar, wl, dev, stream, calls):
@@ -342,10 +355,12 @@ def ll_fused_row(torch, sar, wl, dev, stream, calls):
         ctrl[0] = epoch[0]
         g_ms = time_graph(torch, device_epoch_call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    want = rsag_result(torch, sar, din, wl, stream)
+    same = all(torch.equal(t, want) for t in dout)
     return {"workload": wl.name + "_fused", "calls": calls, "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
             "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
-            "epochs_on_device": int(ctrl[0].item()), "status_ok": ok}
+            "epochs_on_device": int(ctrl[0].item()), "status_ok": ok, "outputs_ok": same}
 
 
 def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
@@ -377,11 +392,13 @@ def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
         ctrl[0] = epoch[0]
         g_ms = time_graph(torch, device_epoch_call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    want = rsag_result(torch, sar, din, wl, stream)
+    same = all(torch.equal(t, want) for t in dout)
     mode = "multi_dest" if multi_dest else "own_output"
     return {"workload": f"{wl.name}_writeback_{mode}", "calls": calls, "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
             "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
-            "status_ok": ok}
+            "status_ok": ok, "outputs_ok": same}
 
 
 def convert_row(torch, sar, dev, stream, count=1 << 26):

@@ -61,3 +61,16 @@ def test_gpu_arm_line():
     assert d["gpu_launches"] == 5
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert d["cpu_baseline"] is None
+
+
+@pytest.mark.gpu
+def test_gpu_ll_rows_match_rsag():
+    """Every LL row at 1 KiB per rank (two-launch, double-buffered on two
+    streams, fused, and both packet write-backs; fp32 and bf16): the status
+    word is clean and the outputs equal the rsag allreduce of the same inputs."""
+    d = _line(["--steps", "3", "--warmup", "3", "--settle-s", "0", "--no-cpu-baseline", "--rows-only", "^ll_8x1KiB_"],
+              timeout=900)
+    rows = d["rows"]
+    assert len(rows) == 10
+    for r in rows:
+        assert r["status_ok"] and r["outputs_ok"], r["workload"]
