@@ -106,9 +106,10 @@ template <int DT> __device__ __forceinline__ void store_bits(void* base, size_t 
     else static_cast<unsigned char*>(base)[i] = static_cast<unsigned char>(word >> (8 * e));
 }
 
-// Phase A: rank r's input -> pkts[r].
+// Phase A: rank r's input -> pkts[r].  x0 is this thread's first input vector,
+// already loaded when tid < nbytes / 16 and the input is 16-byte aligned.
 __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t epoch, bool in16, bool pk32,
-                                     size_t tid, size_t stride) {
+                                     size_t tid, size_t stride, const uint4& x0) {
     const int r = blockIdx.y;
     const size_t npk = (nbytes + 3) / 4;
     uint64_t* mine = a.pkts[r];
@@ -116,7 +117,7 @@ __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t ep
     if (in16) {
         const uint4* src = static_cast<const uint4*>(a.data.in[r]);
         for (size_t q = tid; q < nfull; q += stride) {
-            const uint4 x = ld_stream(src + q);
+            const uint4 x = q == tid ? x0 : ld_stream(src + q);
             const uint64_t p0 = make_packet(x.x, epoch), p1 = make_packet(x.y, epoch);
             const uint64_t p2 = make_packet(x.z, epoch), p3 = make_packet(x.w, epoch);
             if (pk32) {
@@ -241,6 +242,11 @@ __global__ void __launch_bounds__(kThreads)
 coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk, uint32_t host_epoch,
             uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
     pdl_wait();
+    const size_t tid = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    // The first input vector is loaded before the epoch is known, so that
+    // load and the control-block read are in flight together.
+    uint4 x0 = make_uint4(0, 0, 0, 0);
+    if (in16 && tid < nbytes / 16) x0 = ld_stream(static_cast<const uint4*>(a.data.in[blockIdx.y]) + tid);
     __shared__ uint32_t s_epoch;
     if (threadIdx.x == 0) {
         uint32_t e = host_epoch;
@@ -252,10 +258,9 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
     }
     __syncthreads();
     const uint32_t epoch = s_epoch;
-    const size_t tid = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
     const int n = ranks<NR>(n_rt);
-    send(a, nbytes, epoch, in16, pk32, tid, stride);
+    send(a, nbytes, epoch, in16, pk32, tid, stride, x0);
     bool ok = reduce<DT, NR, WB>(a, n_rt, count, nbytes, chunk, epoch, max_spins, status, out16, tid, stride);
     const size_t npk = (nbytes + 3) / 4;
     if constexpr (WB == kPacketsAll) {
@@ -275,16 +280,18 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
                                out16, tid, stride);
     }
     if (ctrl != nullptr) {
-        // Every block read ctrl[0] before arriving; the last block to arrive
-        // publishes the epoch and resets the arrival count for the next launch.
+        // Every block read ctrl[0] before arriving (the add releases that read
+        // and acquires the earlier arrivals); the last block to arrive
+        // publishes the epoch and resets the arrival count for the next launch,
+        // which reads it only after this launch has completed.
         __syncthreads();
         if (threadIdx.x == 0) {
-            __threadfence();
             const uint32_t total = gridDim.x * gridDim.y;
-            if (atomicAdd(ctrl + 1, 1u) == total - 1) {
+            uint32_t prev;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctrl + 1) : "memory");
+            if (prev == total - 1) {
                 ctrl[1] = 0;
                 ctrl[0] = epoch;
-                __threadfence();
             }
         }
     }
@@ -318,7 +325,10 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
         blocks = sms * per_sm;
         resident[dev].store(blocks, std::memory_order_relaxed);
     }
-    size_t want = std::max<size_t>(div_up(in16 ? nbytes / 16 + 4 : npk, kThreads), div_up(chunk, kThreads));
+    // (The up to 3 packets after the last whole 16 input bytes go to threads
+    // 0..2 of a rank's first block, so they need no block of their own: an
+    // idle extra block cost 1.4 us per call at 8 x 4 KiB.)
+    size_t want = std::max<size_t>(div_up(in16 ? nbytes / 16 : npk, kThreads), div_up(chunk, kThreads));
     if (WB == kPacketsOwn) want = std::max<size_t>(want, div_up((npk + 3) / 4, kThreads));
     const size_t cap = static_cast<size_t>(blocks) / nranks;
     if (cap == 0) return cudaErrorCooperativeLaunchTooLarge;
