@@ -176,8 +176,10 @@ SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype);
  * Packet w of rank r (mscclpp commit history, allreduce_allpair_packet fix;
  * layout: 4-byte payload + 4-byte flag): bytes 0..3 are bytes 4w..4w+3 of
  * in[r] (zero past the end of the input), bytes 4..7 the epoch as a
- * little-endian uint32.  Each packet is written with one 8-byte store and read
- * with one 8-byte load, so a reader that sees the flag also sees the payload.
+ * little-endian uint32.  Each packet is written and read as one
+ * single-copy-atomic 8-byte access (alone, or as an element of a 16- or
+ * 32-byte vector access), so a reader that sees the flag also sees the
+ * payload.
  *
  * Packet buffers belong to the caller, must be 16-byte aligned, and must be
  * zeroed once before first use: epoch 0 is reserved for "never written"
@@ -197,11 +199,11 @@ SAR_API sar_status sar_ll_pack(const void* const* in, void* const* pkts, int nra
 /*
  * sar_ll_unpack_reduce -- the LL reduce and write-back.
  *
- * Simulated rank r owns a 1/N chunk of the packet index range (whole groups of
- * 4 packets).  For each packet in it, for k = 0..N-1 in order, it loads
- * pkts[k]'s packet, polls until the flag equals `epoch`, adds the payload's
- * elements in binary32, rounds once and stores the elements to all N outputs.
- * The values equal sar_allreduce's.
+ * Simulated rank r owns a 1/N chunk of the packet index range (ceil(P / N)
+ * packets of the P per buffer).  For each packet in it, for k = 0..N-1 in
+ * order, it loads pkts[k]'s packet, polls until the flag equals `epoch`, adds
+ * the payload's elements in binary32, rounds once and stores the elements to
+ * all N outputs.  The values equal sar_allreduce's.
  *
  * A poll re-reads a packet at most `max_spins` times (with a short sleep
  * between reads).  When one runs out, the kernel stores SAR_ERR_TIMEOUT into
