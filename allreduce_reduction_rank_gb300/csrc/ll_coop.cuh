@@ -74,12 +74,13 @@ __device__ __forceinline__ bool poll(const uint64_t* src, uint32_t epoch, uint64
             atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
             return false;
         }
-        if (ld_status_v(status) != 0) return false;
         // The packets come from other blocks of this launch, usually within a
         // few hundred cycles: re-read at once for the first polls, then back
         // off (measured: 3-15% faster from 4 KiB per rank up than sleeping
-        // from the first miss).
+        // from the first miss).  Only a thread that has started to back off
+        // looks at the shared status word.
         if (spin >= kSpinPolls) {
+            if (ld_status_v(status) != 0) return false;
             __nanosleep(ns);
             if (ns < kMaxSleepNs) ns *= 2;
         }
