@@ -7,7 +7,7 @@
 // 8-byte store, so a reader that sees the flag also sees the payload.
 //
 //   pack          : rank r's input -> packets in pkts[r], flag = epoch
-//   unpack_reduce : rank r polls packet group q of every rank k = 0..N-1 (in
+//   unpack_reduce : rank r polls packet w of every rank k = 0..N-1 (in
 //                   order) until the flags equal epoch, adds the payloads in
 //                   binary32, rounds once and writes the elements to all N
 //                   outputs.

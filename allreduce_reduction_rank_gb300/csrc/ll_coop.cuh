@@ -326,8 +326,8 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
         blocks = sms * per_sm;
         resident[dev].store(blocks, std::memory_order_relaxed);
     }
-    // (The up to 3 packets after the last whole 16 input bytes go to threads
-    // 0..2 of a rank's first block, so they need no block of their own: an
+    // (The up to 4 packets after the last whole 16 input bytes go to threads
+    // 0..3 of a rank's first block, so they need no block of their own: an
     // idle extra block cost 1.4 us per call at 8 x 4 KiB.)
     size_t want = std::max<size_t>(div_up(in16 ? nbytes / 16 : npk, kThreads), div_up(chunk, kThreads));
     if (WB == kPacketsOwn) want = std::max<size_t>(want, div_up((npk + 3) / 4, kThreads));
