@@ -7,7 +7,7 @@
 // memory budget, or code paths where a cudaMalloc would synchronise the device
 // or is not allowed at all.  This entry point takes the scratch from a fixed
 // array compiled into the library instead, so the call itself allocates
-// nothing.  The paper has no counterpart of this entry point.
+// nothing.  MSCCL++ has no counterpart of this entry point.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library's device code reserves it and holds it until the process exits.  In

@@ -313,7 +313,7 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
  * scratch, for callers that cannot allocate device memory: code inside a
  * framework whose allocator owns the device memory, plugins with a fixed
  * memory budget, or paths where a cudaMalloc would synchronise the device or
- * is not allowed.  The paper has no counterpart of this entry point.
+ * is not allowed.  MSCCL++ has no counterpart of this entry point.
  *
  * The outputs equal sar_allreduce_ll's bit for bit.  The call allocates
  * nothing: the packet scratch is a fixed array of SAR_LL_NOALLOC_SCRATCH_BYTES
