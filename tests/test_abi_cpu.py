@@ -185,3 +185,61 @@ def test_double_buffer_halves_stay_16_byte_aligned(sar, dt):
         pb = sar.sar_ll_packet_bytes(count, dt)
         total = sar.ll_double_packet_bytes(count, dt)
         assert total % 32 == 0 and total >= 2 * pb and total - 2 * pb < 32
+
+
+C_PROGRAM = r"""
+#include "sar.h"
+#include <stdio.h>
+#include <string.h>
+
+static int bad = 0;
+#define EXPECT(call, want)                                                              \
+    do {                                                                                \
+        sar_status got_ = (call);                                                       \
+        if (got_ != (want)) {                                                           \
+            printf("%s -> %d, want %d\n", #call, (int)got_, (int)(want));               \
+            bad = 1;                                                                    \
+        }                                                                               \
+    } while (0)
+
+int main(void) {
+    const void* in[2] = {(const void*)(uintptr_t)4096, (const void*)(uintptr_t)8192};
+    void* out[2] = {(void*)(uintptr_t)4096, (void*)(uintptr_t)8192};
+    EXPECT(sar_allreduce(in, out, 0, 16, SAR_BF16, SAR_ALGO_RSAG, NULL), SAR_ERR_UNSUPPORTED_NRANKS);
+    EXPECT(sar_allreduce(in, out, 2, 16, (sar_dtype)5, SAR_ALGO_RSAG, NULL), SAR_ERR_UNSUPPORTED_DTYPE);
+    EXPECT(sar_allreduce(in, out, 2, 0, SAR_BF16, SAR_ALGO_RSAG, NULL), SAR_OK);
+    EXPECT(sar_ll_pack(in, out, 2, 16, SAR_BF16, 0, NULL), SAR_ERR_INVALID_ARG);
+    EXPECT(sar_read_device_status(NULL, NULL), SAR_ERR_INVALID_ARG);
+    if (sar_ll_packet_bytes(5, SAR_FP32) != 40) {
+        printf("sar_ll_packet_bytes(5, fp32) = %zu\n", sar_ll_packet_bytes(5, SAR_FP32));
+        bad = 1;
+    }
+    if (strncmp(sar_status_string(SAR_ERR_TIMEOUT), "SAR_ERR_TIMEOUT", 15) != 0) {
+        printf("status string: %s\n", sar_status_string(SAR_ERR_TIMEOUT));
+        bad = 1;
+    }
+    printf(bad ? "FAIL\n" : "OK\n");
+    return bad;
+}
+"""
+
+
+def test_plain_c_program_uses_the_boundary(sar, tmp_path):
+    """A C11 program that includes only sar.h (no CUDA or C++ header) compiles
+    with -Wall -Wextra -pedantic -Werror, links against libsar.so, and gets
+    the argument errors back before any launch, so it needs no GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src, exe = tmp_path / "use_sar.c", tmp_path / "use_sar"
+    src.write_text(C_PROGRAM)
+    libdir = os.path.dirname(sar.LIB_PATH)
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    build = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", include, str(src),
+                            "-L", libdir, "-lsar", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                           capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip() == "OK", run.stdout + run.stderr
