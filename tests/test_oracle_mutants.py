@@ -1,7 +1,8 @@
 """The oracle's pins have teeth: plausible mistakes planted in a copy of the
 oracle source (a wrong tie rule, a dropped rank, a reversed rank order, a
 lost sign, an off-by-one bias, a missing saturation, a wrong packet layout, an
-unrounded chunk size, a zero seed) must each fail at least one pin.
+unrounded chunk size, a zero seed, an unpack that ignores the epoch or reads
+the wrong half of a packet) must each fail at least one pin.
 
 Mistakes are planted only in a temporary copy of the C oracle, on the CPU.
 """
@@ -60,6 +61,10 @@ MUTANTS = {
         ("        mag = ldexpf((float)f, -17);", "        mag = ldexpf((float)f, -16);"),
     "all-gather skips a peer":
         ("if (j == r || e == b) continue;", "if (j == r || j == 0 || e == b) continue;"),
+    "unpack accepts any flag":
+        ("if (flag != epoch) return ORC_NOT_ARRIVED;", "(void)flag;"),
+    "unpack reads the payload from the flag half":
+        ("rebuilt[r][at] = p[8 * (at / 4) + at % 4];", "rebuilt[r][at] = p[8 * (at / 4) + 4 + at % 4];"),
 }
 
 
@@ -78,6 +83,8 @@ def _battery(points):
         lambda: [ts.test_rsag_chunks_partition_the_range(d) for d in ts.DTYPES],
         lambda: [ts.test_reduce_scatter_then_all_gather_is_allreduce(d, 8, 4097) for d in ts.DTYPES],
         lambda: [ts.test_ll_pack_byte_image(d, 5) for d in ts.DTYPES],
+        lambda: [ts.test_ll_unpack_reduce_gives_the_exact_sums(d, 8, 257) for d in ts.DTYPES],
+        lambda: ts.test_ll_stale_flag_is_not_arrived(),
         lambda: [ta.test_stepwise_reference(d, a, 8) for d, a in ta.CASES],
         lambda: ta.test_native_e4m3fn_rounds_every_partial_sum(),
     ]
