@@ -267,8 +267,10 @@ SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* o
  * stores it, so a launch captured in a CUDA graph gets a fresh epoch on every
  * replay; `epoch` is then ignored.  Packet buffers, max_spins and d_status as
  * in sar_ll_unpack_reduce, except that the first 16 re-reads of a packet come
- * without a sleep (the packets are written by the same launch).  One control
- * block must not be shared by launches that can overlap on the GPU.
+ * without a sleep (the packets are written by the same launch), and a thread
+ * looks at *d_status (to stop when another has given up) only after them.
+ * One control block must not be shared by launches that can overlap on the
+ * GPU.
  */
 SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,
                                           size_t count, sar_dtype dtype, uint32_t epoch, uint32_t* d_epoch,
