@@ -47,6 +47,8 @@ enum WriteBack { kDirect = 0, kPacketsAll = 1, kPacketsOwn = 2 };
 
 constexpr unsigned kMaxSleepNs = 1024;
 constexpr uint64_t kSpinPolls = 16;
+// Input vectors a send thread loads before it stores their packets.
+constexpr int kSendBatch = 4;
 
 __device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
     int32_t v;
@@ -93,6 +95,40 @@ __device__ __forceinline__ bool poll(const uint64_t* src, uint32_t epoch, uint64
     }
 }
 
+// Wait until packet w of every rank k0 .. k0 + WIN - 1 (below n; already
+// loaded into pk) carries `epoch`.  Every stale packet of the window is
+// re-read in the same step, so a step costs one memory round trip whatever
+// the rank count (re-reading the ranks one after another cost one round trip
+// per stale rank).  False when this thread gave up or saw another give up.
+template <int WIN, int NR>
+__device__ __forceinline__ bool poll_window(uint64_t* const* pkts, int k0, int n, size_t w, uint32_t epoch,
+                                            uint64_t max_spins, int32_t* status, uint64_t (&pk)[WIN]) {
+    unsigned ns = 32;
+    for (uint64_t spin = 0;; ++spin) {
+        bool ready = true;
+#pragma unroll
+        for (int k = 0; k < WIN; ++k) {
+            if (NR == 0 && k0 + k >= n) break;
+            ready = ready && packet_flag(pk[k]) == epoch;
+        }
+        if (ready) return true;
+        if (spin >= max_spins) {
+            atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+            return false;
+        }
+        if (spin >= kSpinPolls) {
+            if (ld_status_v(status) != 0) return false;
+            __nanosleep(ns);
+            if (ns < kMaxSleepNs) ns *= 2;
+        }
+#pragma unroll
+        for (int k = 0; k < WIN; ++k) {
+            if (NR == 0 && k0 + k >= n) break;
+            if (packet_flag(pk[k]) != epoch) pk[k] = ld_packet(pkts[k0 + k] + w);
+        }
+    }
+}
+
 struct LLArgs {
     RankPtrs data;                   // in[r]: inputs, out[j]: outputs
     uint64_t* pkts[SAR_MAX_RANKS];   // send packet buffers
@@ -117,15 +153,31 @@ __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t ep
     const size_t nfull = nbytes / 16;
     if (in16) {
         const uint4* src = static_cast<const uint4*>(a.data.in[r]);
-        for (size_t q = tid; q < nfull; q += stride) {
-            const uint4 x = q == tid ? x0 : ld_stream(src + q);
-            const uint64_t p0 = make_packet(x.x, epoch), p1 = make_packet(x.y, epoch);
-            const uint64_t p2 = make_packet(x.z, epoch), p3 = make_packet(x.w, epoch);
-            if (pk32) {
-                st_packets4(mine + 4 * q, p0, p1, p2, p3);
-            } else {
-                st_packets2(mine + 4 * q, p0, p1);
-                st_packets2(mine + 4 * q + 2, p2, p3);
+        // A thread's vectors q0, q0 + stride, ... are loaded kSendBatch at a
+        // time before any of them is stored (the packet stores are ordered
+        // memory operations that later loads may not pass), so one memory
+        // round trip covers a batch.
+        for (size_t q0 = tid; q0 < nfull; q0 += kSendBatch * stride) {
+            uint4 x[kSendBatch];
+#pragma unroll
+            for (int u = 0; u < kSendBatch; ++u) {
+                const size_t q = q0 + u * stride;
+                x[u] = make_uint4(0, 0, 0, 0);
+                if (u == 0 && q0 == tid) x[u] = x0;
+                else if (q < nfull) x[u] = ld_stream(src + q);
+            }
+#pragma unroll
+            for (int u = 0; u < kSendBatch; ++u) {
+                const size_t q = q0 + u * stride;
+                if (q >= nfull) break;
+                const uint64_t p0 = make_packet(x[u].x, epoch), p1 = make_packet(x[u].y, epoch);
+                const uint64_t p2 = make_packet(x[u].z, epoch), p3 = make_packet(x[u].w, epoch);
+                if (pk32) {
+                    st_packets4(mine + 4 * q, p0, p1, p2, p3);
+                } else {
+                    st_packets2(mine + 4 * q, p0, p1);
+                    st_packets2(mine + 4 * q + 2, p2, p3);
+                }
             }
         }
     }
@@ -155,18 +207,18 @@ __device__ __forceinline__ bool reduce(const LLArgs& a, int n_rt, size_t count, 
         float acc[EP];
 #pragma unroll 1
         for (int k0 = 0; k0 < n; k0 += WIN) {
-            uint64_t pk[WIN][1];
+            uint64_t pk[WIN];
 #pragma unroll
             for (int k = 0; k < WIN; ++k) {
                 if (NR == 0 && k0 + k >= n) break;
-                pk[k][0] = ld_packet(a.pkts[k0 + k] + w);
+                pk[k] = ld_packet(a.pkts[k0 + k] + w);
             }
+            if (!poll_window<WIN, NR>(a.pkts, k0, n, w, epoch, max_spins, status, pk)) return false;
 #pragma unroll
             for (int k = 0; k < WIN; ++k) {
                 if (NR == 0 && k0 + k >= n) break;
-                if (!poll<1>(a.pkts[k0 + k] + w, epoch, max_spins, status, pk[k])) return false;
                 float x[EP];
-                widen_word<DT>(packet_payload(pk[k][0]), x);
+                widen_word<DT>(packet_payload(pk[k]), x);
 #pragma unroll
                 for (int e = 0; e < EP; ++e) acc[e] = (k0 + k == 0) ? x[e] : __fadd_rn(acc[e], x[e]);
             }
