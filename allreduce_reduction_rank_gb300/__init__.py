@@ -36,7 +36,7 @@ lib = ctypes.CDLL(LIB_PATH)
 # sar_dtype
 SAR_BF16, SAR_FP16, SAR_FP32, SAR_FP8_E4M3FN, SAR_FP8_E4M3B15 = 0, 1, 2, 3, 4
 # sar_algo
-SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE = 0, 1
+SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE, SAR_ALGO_LL_ALLPAIR = 0, 1, 2
 # sar_status
 (SAR_OK, SAR_ERR_INVALID_ARG, SAR_ERR_UNSUPPORTED_NRANKS, SAR_ERR_UNSUPPORTED_DTYPE,
  SAR_ERR_MISALIGNED, SAR_ERR_CUDA, SAR_ERR_TIMEOUT) = range(7)
@@ -158,7 +158,9 @@ def sar_ll_packet_bytes(count: int, dtype) -> int:
 
 
 def sar_allreduce(ins, outs, count=None, dtype=None, algo=SAR_ALGO_RSAG, stream=None) -> None:
-    """rsag allreduce: every outs[j] = R(sum over ranks 0..N-1 of ins[k])."""
+    """Allreduce: every outs[j] = R(sum over ranks 0..N-1 of ins[k]), by the
+    rsag kernels or (SAR_ALGO_LL_ALLPAIR) the LL packets on the library's
+    fixed scratch."""
     pin, n = _ptrs(ins)
     pout, n_out = _ptrs(outs)
     if n != n_out:
@@ -261,6 +263,25 @@ def sar_allreduce_ll_noalloc(ins, outs, status=None, max_spins: int = 1 << 20, c
     pout, _ = _ptrs(outs)
     _check(lib.sar_allreduce_ll_noalloc(pin, pout, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), max_spins,
                                         None if status is None else _addr(status), _stream(stream)))
+
+
+# The device epoch counter of sar_allreduce_ll_fused / _writeback: one uint64,
+# launches so far in bits 20..63.
+LL_EPOCH_SHIFT = 20
+_EPOCH_PERIOD = 0xFFFFFFFF
+
+
+def ll_device_epoch(ctrl) -> int:
+    """The epoch the last launch on a device epoch counter used (0 before the
+    first launch); ctrl is an 8-byte CUDA tensor.  Synchronises."""
+    launches = int(ctrl.view(torch.int64)[0].item()) >> LL_EPOCH_SHIFT
+    return 0 if launches == 0 else (launches - 1) % _EPOCH_PERIOD + 1
+
+
+def ll_set_device_epoch(ctrl, last_epoch: int) -> None:
+    """Make the next launch on the counter use last_epoch + 1 (1 after
+    2^32 - 1), for example to continue after host epochs 1..last_epoch."""
+    ctrl.view(torch.int64)[0] = int(last_epoch) << LL_EPOCH_SHIFT
 
 
 def sar_fp8_convert(src, dst, src_dtype=None, dst_dtype=None, count=None, stream=None) -> None:

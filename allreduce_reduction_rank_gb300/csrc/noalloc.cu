@@ -32,24 +32,38 @@ static __device__ __align__(256) unsigned char g_ll_scratch[SAR_LL_NOALLOC_SCRAT
 constexpr int kMaxDevices = 64;
 
 struct DeviceScratch {
-    std::once_flag once;
-    unsigned char* base = nullptr;   // device address of g_ll_scratch on this device
-    cudaError_t err = cudaSuccess;
-    std::atomic<uint32_t> epoch{0};  // last epoch used on this device
+    std::mutex mu;
+    std::atomic<unsigned char*> base{nullptr};   // device address of g_ll_scratch on this device
+    std::atomic<uint32_t> epoch{0};               // last epoch used on this device
 };
 
 DeviceScratch g_dev[kMaxDevices];
 
-// Device address of the scratch on the current device (set up on first use).
+// Device address of the scratch on the current device, looked up on first
+// use.  Only a successful lookup is kept: after a failure (for example a first
+// call made during a CUDA graph capture) the next call tries again.
 cudaError_t scratch_base(int dev, unsigned char** out) {
     DeviceScratch& d = g_dev[dev];
-    std::call_once(d.once, [&d]() {
-        void* p = nullptr;
-        d.err = cudaGetSymbolAddress(&p, g_ll_scratch);
-        d.base = static_cast<unsigned char*>(p);
-    });
-    *out = d.base;
-    return d.err;
+    unsigned char* b = d.base.load(std::memory_order_acquire);
+    if (b == nullptr) {
+        std::lock_guard<std::mutex> lock(d.mu);
+        b = d.base.load(std::memory_order_relaxed);
+        if (b == nullptr) {
+            void* p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_ll_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                // Reported here; cleared so that a later launch check does not
+                // report it again.
+                (void)cudaGetLastError();
+                *out = nullptr;
+                return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            }
+            b = static_cast<unsigned char*>(p);
+            d.base.store(b, std::memory_order_release);
+        }
+    }
+    *out = b;
+    return cudaSuccess;
 }
 
 bool supported(int n) { return n >= 1 && n <= SAR_MAX_RANKS; }
@@ -57,13 +71,10 @@ bool supported(int n) { return n >= 1 && n <= SAR_MAX_RANKS; }
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
-}  // namespace sar
 
-using namespace sar;
-
-extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, void* const* out, int nranks,
-                                                       size_t count, sar_dtype dtype, uint64_t max_spins,
-                                                       int32_t* d_status, sar_stream_t stream) {
+sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
+                                      sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
+                                      bool clear_internal_status, cudaStream_t s) {
     if (!supported(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
     if (dtype < SAR_BF16 || dtype > SAR_FP8_E4M3B15) return SAR_ERR_UNSUPPORTED_DTYPE;
     if (in == nullptr || out == nullptr || max_spins == 0) return SAR_ERR_INVALID_ARG;
@@ -87,7 +98,6 @@ extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, vo
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SAR_ERR_CUDA;
     unsigned char* base = nullptr;
     if (scratch_base(dev, &base) != cudaSuccess || base == nullptr) return SAR_ERR_CUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // A fresh epoch per call on this device, so packets left in the shared
     // array by an earlier call never match.  After 2^32 - 1 calls the epoch
@@ -99,9 +109,10 @@ extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, vo
     }
     int32_t* status = d_status;
     if (status == nullptr) {
-        // The internal status word keeps the last call's value: clear it.
         status = reinterpret_cast<int32_t*>(base + SAR_LL_NOALLOC_SCRATCH_BYTES);
-        if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SAR_ERR_CUDA;
+        // The internal status word keeps the last call's value.
+        if (clear_internal_status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess)
+            return SAR_ERR_CUDA;
     }
 
     RankPtrs pack, unpack;
@@ -118,4 +129,21 @@ extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, vo
     if (launch_ll_unpack_reduce(dtype, nranks, unpack, count, epoch, max_spins, status, out16, s) != cudaSuccess)
         return SAR_ERR_CUDA;
     return SAR_OK;
+}
+
+unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoch) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (set_epoch) g_dev[dev].epoch.store(last_epoch);
+    return g_dev[dev].base.load();
+}
+
+}  // namespace sar
+
+extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, void* const* out, int nranks,
+                                                       size_t count, sar_dtype dtype, uint64_t max_spins,
+                                                       int32_t* d_status, sar_stream_t stream) {
+    // Without a caller status word the internal one is cleared first, so that
+    // a timeout of an earlier call does not end this call's polls at once.
+    return sar::ll_fixed_scratch_allreduce(in, out, nranks, count, dtype, max_spins, d_status, true,
+                                           reinterpret_cast<cudaStream_t>(stream));
 }

@@ -37,6 +37,10 @@ bool valid_dtype(int dt) { return dt >= SAR_BF16 && dt <= SAR_FP8_E4M3B15; }
 
 bool is_fp8(int dt) { return dt == SAR_FP8_E4M3FN || dt == SAR_FP8_E4M3B15; }
 
+// Poll bound of sar_allreduce with SAR_ALGO_LL_ALLPAIR (re-reads of one packet,
+// with sleeps of up to about a microsecond between them).
+constexpr uint64_t kFixedScratchSpins = uint64_t(1) << 20;
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Checks nranks device pointers: non-NULL and aligned to `align`; clears
@@ -201,6 +205,14 @@ SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype) {
 
 SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
                                  sar_dtype dtype, sar_algo algo, sar_stream_t stream) {
+    if (algo == SAR_ALGO_LL_ALLPAIR) {
+        // Two launches in stream order, so no poll ever waits; the bound only
+        // ends polls of calls that race on the shared scratch.  Their timeout
+        // goes to the internal status word, which nothing reads, so it is not
+        // cleared per call.
+        return ll_fixed_scratch_allreduce(in, out, nranks, count, dtype, kFixedScratchSpins, nullptr, false,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    }
     if (algo != SAR_ALGO_RSAG && algo != SAR_ALGO_RSAG_TWO_PHASE) {
         if (!supported_nranks(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
         return SAR_ERR_INVALID_ARG;
@@ -309,7 +321,7 @@ SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* o
 }
 
 SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,
-                                          size_t count, sar_dtype dtype, uint32_t epoch, uint32_t* d_epoch,
+                                          size_t count, sar_dtype dtype, uint32_t epoch, uint64_t* d_epoch,
                                           uint64_t max_spins, int32_t* d_status, sar_stream_t stream) {
     bool launch = false, in16 = false, out16 = false;
     // With a device epoch counter the host epoch is unused; any non-zero value
@@ -333,7 +345,7 @@ SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* ou
 
 SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const* out, void* const* pkts, void* res,
                                               int nranks, size_t count, sar_dtype dtype, uint32_t epoch,
-                                              uint32_t* d_epoch, int multi_dest, uint64_t max_spins,
+                                              uint64_t* d_epoch, int multi_dest, uint64_t max_spins,
                                               int32_t* d_status, sar_stream_t stream) {
     bool launch = false, in16 = false, out16 = false;
     sar_status st = check_ll(in, pkts, nranks, count, dtype, d_epoch != nullptr ? 1u : epoch, &launch, &in16);

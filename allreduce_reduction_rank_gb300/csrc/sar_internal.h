@@ -78,16 +78,30 @@ cudaError_t launch_ll_unpack_reduce(sar_dtype dt, int nranks, const RankPtrs& p,
                                     bool vec_out, cudaStream_t stream);
 
 // LL send + reduce + write-back in one cooperative launch.  ctrl: optional
-// device {last epoch, arrivals}; with it the epoch is ctrl[0] + 1.
+// device epoch counter (launches << 20); with it the k-th launch uses epoch
+// (k mod (2^32 - 1)) + 1.
 cudaError_t launch_ll_fused(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, size_t count,
-                            uint32_t epoch, uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16,
+                            uint32_t epoch, uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16,
                             bool out16, cudaStream_t stream);
 
 // LL with the write-back as a second packet round into `res`; multi_dest:
 // each result packet is read once and written to all outputs.
 cudaError_t launch_ll_writeback(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, void* res,
-                                size_t count, uint32_t epoch, uint32_t* ctrl, bool multi_dest, uint64_t max_spins,
+                                size_t count, uint32_t epoch, uint64_t* ctrl, bool multi_dest, uint64_t max_spins,
                                 int32_t* status, bool in16, bool out16, cudaStream_t stream);
+
+// The LL allreduce (pack, then unpack-reduce) on the packet scratch compiled
+// into the library (noalloc.cu), with a fresh epoch per call and device.
+// d_status == nullptr: the internal status word, cleared first when
+// clear_internal_status.  Validates its arguments itself.
+sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
+                                      sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
+                                      bool clear_internal_status, cudaStream_t stream);
+
+// Test support for the fixed scratch (not exported from the library; a test
+// program links the object files): sets the last epoch used on `dev` and
+// returns the array's device address there (nullptr if it was not looked up).
+unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoch);
 
 cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
                            size_t count, bool vec, cudaStream_t stream);

@@ -86,12 +86,10 @@ typedef enum {
                             overflow rounds to inf, subnormals m/8 * 2^-14 */
 } sar_dtype;
 
-/* The LL all-pair allreduce is not a sar_algo: it needs a packet scratch, an
- * epoch and a device status word, which sar_allreduce has no arguments for.
- * It has its own entry points (sar_allreduce_ll and its variants below). */
 typedef enum {
     SAR_ALGO_RSAG = 0,            /* one fused kernel: reduce chunk, write to all outputs */
-    SAR_ALGO_RSAG_TWO_PHASE = 1   /* reduce-scatter kernel, then all-gather kernel */
+    SAR_ALGO_RSAG_TWO_PHASE = 1,  /* reduce-scatter kernel, then all-gather kernel */
+    SAR_ALGO_LL_ALLPAIR = 2       /* LL all-pair packets on the library's fixed scratch */
 } sar_algo;
 
 typedef enum {
@@ -120,7 +118,23 @@ typedef enum {
  * C = sar_rsag_chunk(count, nranks, dtype).  SAR_ALGO_RSAG reduces each chunk
  * and writes it to all N outputs in one kernel (N*S bytes read, N*S written,
  * S = count * element size).  SAR_ALGO_RSAG_TWO_PHASE runs sar_reduce_scatter
- * then sar_all_gather.  Both give the same bits.
+ * then sar_all_gather.
+ *
+ * SAR_ALGO_LL_ALLPAIR runs the LL all-pair allreduce (mscclpp commit history,
+ * the allreduce_allpair_packet fix): sar_ll_pack then sar_ll_unpack_reduce,
+ * stream-ordered, on the packet scratch compiled into the library (the array
+ * that sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  It
+ * therefore takes only the sizes that fit that array (nranks *
+ * sar_ll_packet_bytes(count, dtype) rounded up to 256 bytes per rank at most
+ * SAR_LL_NOALLOC_SCRATCH_BYTES, e.g. up to 1 MiB per rank with 8 ranks);
+ * larger calls return SAR_ERR_INVALID_ARG before any launch.  The first
+ * LL_ALLPAIR or noalloc call on a device looks up the array's address; make
+ * it before any CUDA graph capture on that device.  In stream order every
+ * packet a call polls was written by the same call's pack kernel, so the
+ * polls never wait.  Calls that overlap on the GPU (two streams without
+ * ordering) share the array and race: their outputs are undefined.
+ *
+ * All three algorithms give the same bits.
  *
  * in, out : host arrays of `nranks` device pointers, `count` elements each,
  *           dense.  out[r] == in[r] (in place) is allowed; any other overlap
@@ -261,19 +275,34 @@ SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* o
  * SAR_ERR_CUDA.
  *
  * Epoch: with d_epoch == NULL the caller's `epoch` (non-zero, as in
- * sar_ll_pack).  Otherwise d_epoch is a caller-owned device control block of
- * two uint32 {last epoch, arrivals}, 8-byte aligned, zeroed once before first
- * use: each launch uses last + 1 (skipping 0) and the last block to finish
- * stores it, so a launch captured in a CUDA graph gets a fresh epoch on every
- * replay; `epoch` is then ignored.  Packet buffers, max_spins and d_status as
- * in sar_ll_unpack_reduce, except that the first 16 re-reads of a packet come
- * without a sleep (the packets are written by the same launch), and a thread
- * looks at *d_status (to stop when another has given up) only after them.
- * One control block must not be shared by launches that can overlap on the
- * GPU.
+ * sar_ll_pack).  Otherwise d_epoch is a caller-owned device epoch counter:
+ * 8 bytes, 8-byte aligned, zeroed once before first use, read and written by
+ * the kernels as one uint64 (little-endian) whose bits 20..63 count the
+ * launches that used it (bits 0..19 are zero between launches).  The k-th
+ * launch (k = 0, 1, ...) uses epoch (k mod (2^32 - 1)) + 1, so a launch
+ * captured in a CUDA graph gets a fresh epoch on every replay; `epoch` is
+ * then ignored.  To continue after host epochs 1..e, store (uint64)e << 20.
+ * Every block takes the epoch with one atomic add at its start; no block
+ * waits for another and nothing is written at the end of the launch.  One
+ * counter must not be shared by launches that can overlap on the GPU.
+ *
+ * Epochs repeat every 2^32 - 1 launches of one counter.  Each launch writes
+ * all of its packets with the new epoch, and consecutive launches always use
+ * different epochs, so calls with one count per set of buffers never see a
+ * stale packet.  A caller that varies `count` on the same buffers leaves
+ * packets past the smaller calls' ends untouched; it should zero the packet
+ * buffers and the counter at least once every 2^32 - 2 launches (about 2.4
+ * hours of back-to-back 2 us launches), for example by counting the replays
+ * of its graphs.
+ *
+ * Packet buffers, max_spins and d_status as in sar_ll_unpack_reduce, except
+ * that the first 16 re-reads of a packet come without a sleep (the packets
+ * are written by the same launch), and a thread looks at *d_status (to stop
+ * when another has given up) only after them.  A poll that runs out does not
+ * stop the launch from advancing the counter.
  */
 SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* out, void* const* pkts, int nranks,
-                                          size_t count, sar_dtype dtype, uint32_t epoch, uint32_t* d_epoch,
+                                          size_t count, sar_dtype dtype, uint32_t epoch, uint64_t* d_epoch,
                                           uint64_t max_spins, int32_t* d_status, sar_stream_t stream);
 
 /*
@@ -295,11 +324,12 @@ SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* ou
  *
  * res : caller-owned device buffer of sar_ll_packet_bytes(count, dtype) bytes,
  *       16-byte aligned, zeroed once before first use; the same epoch rules as
- *       the send packet buffers.
+ *       the send packet buffers.  d_epoch: the device epoch counter as in
+ *       sar_allreduce_ll_fused (one counter may serve both entry points).
  */
 SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const* out, void* const* pkts, void* res,
                                               int nranks, size_t count, sar_dtype dtype, uint32_t epoch,
-                                              uint32_t* d_epoch, int multi_dest, uint64_t max_spins,
+                                              uint64_t* d_epoch, int multi_dest, uint64_t max_spins,
                                               int32_t* d_status, sar_stream_t stream);
 
 /*
@@ -327,7 +357,8 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
  *   SAR_ERR_INVALID_ARG before anything is launched.
  * - The first call on a device looks up the array's device address on that
  *   device (the current one); make that first call before any CUDA graph
- *   capture on the device.
+ *   capture on the device.  If the lookup fails (SAR_ERR_CUDA), nothing is
+ *   kept and the next call tries again.
  * - The epoch is managed by the library (a new one per call and device).
  * - d_status: an optional caller device int32 that receives SAR_ERR_TIMEOUT if
  *   a poll runs out of spins (as in sar_ll_unpack_reduce).  With NULL, an

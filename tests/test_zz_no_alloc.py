@@ -90,3 +90,25 @@ def test_noalloc_largest_fitting_call(sar):
     assert sar.sar_read_device_status(st) == sar.SAR_OK
     for j in range(n):
         assert np.array_equal(new[j].bytes(), ref[j].bytes())
+
+
+def test_noalloc_epoch_wrap_clears_the_array(sar, tmp_path):
+    """After 2^32 - 1 calls on a device the internal epoch wraps: the call
+    that wraps zeroes the whole array, then uses epoch 1.  A test program
+    linked against the library's object files sets the epoch counter through
+    an internal hook and checks the outputs, the packets' flags and that the
+    bytes past the wrapping call's packets are zero."""
+    import glob
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    objs = sorted(glob.glob(os.path.join(root, "allreduce_reduction_rank_gb300", "_build", "*.o")))
+    assert objs, "library objects missing (build first)"
+    exe = tmp_path / "noalloc_wrap_check"
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    build = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-I",
+                            os.path.join(root, "include"), os.path.join(root, "tests", "noalloc_wrap_check.cu")]
+                           + objs + ["-o", str(exe)], capture_output=True, text=True, timeout=600)
+    assert build.returncode == 0, build.stderr[-3000:]
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    assert run.returncode == 0 and run.stdout.strip().endswith("OK"), run.stdout + run.stderr
