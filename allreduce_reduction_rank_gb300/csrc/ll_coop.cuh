@@ -27,10 +27,9 @@
 // Every poll is bounded.  Blocks wait on one another, so the launch is
 // cooperative: the runtime makes every block co-resident or refuses the launch.
 //
-// Epochs: the caller's, or a device control block {last epoch, arrivals}
-// (commit history, the flag buffer change: one flag buffer shared by the
-// algorithms) that the kernel advances: every launch uses last + 1 and the last
-// block to finish stores it, so a replayed CUDA graph gets a fresh epoch.
+// Epochs: the caller's, or a device counter (commit history, the flag buffer
+// change: one flag buffer shared by the algorithms) that every launch advances
+// by itself (take_ticket), so a replayed CUDA graph gets a fresh epoch.
 #pragma once
 
 #include <algorithm>
@@ -53,11 +52,6 @@ constexpr int kSendBatch = 4;
 __device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
     int32_t v;
     asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_u32_v(const uint32_t* s) {
-    uint32_t v;
-    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
     return v;
 }
 
@@ -127,6 +121,25 @@ __device__ __forceinline__ bool poll_window(uint64_t* const* pkts, int k0, int n
             if (packet_flag(pk[k]) != epoch) pk[k] = ld_packet(pkts[k0 + k] + w);
         }
     }
+}
+
+// The device epoch counter: one uint64 whose bits kTicketBits.. count the
+// launches that used it and whose low bits are zero between launches.  Every
+// block of a launch adds to it once, block (0, 0) 2^kTicketBits - (blocks - 1)
+// and every other block 1, so one launch adds exactly 2^kTicketBits.  The
+// launches of one counter run one after another (stream order), so the value
+// each block gets back lies in [k * 2^kTicketBits, (k + 1) * 2^kTicketBits)
+// for the k-th launch whatever the order of the adds, and every block derives
+// the same epoch (k mod (2^32 - 1)) + 1 from it: never 0, and consecutive
+// launches always differ.  No block waits for another and nothing is written
+// at the end of the launch.
+constexpr int kTicketBits = 20;
+__device__ __forceinline__ uint32_t take_ticket(uint64_t* ctrl) {
+    const uint64_t blocks = static_cast<uint64_t>(gridDim.x) * gridDim.y;
+    const uint64_t inc = (blockIdx.x == 0 && blockIdx.y == 0) ? (uint64_t(1) << kTicketBits) - (blocks - 1) : 1;
+    uint64_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ctrl), "l"(inc) : "memory");
+    return static_cast<uint32_t>((old >> kTicketBits) % 0xFFFFFFFFull) + 1;
 }
 
 struct LLArgs {
@@ -293,7 +306,7 @@ __device__ __forceinline__ bool unpack_results(const LLArgs& a, size_t count, si
 template <int DT, int NR, int WB>
 __global__ void __launch_bounds__(kThreads)
 coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk, uint32_t host_epoch,
-            uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
+            uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
     pdl_wait();
     const size_t tid = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     // The first input vector is loaded before the epoch is known, so that
@@ -303,10 +316,7 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
     __shared__ uint32_t s_epoch;
     if (threadIdx.x == 0) {
         uint32_t e = host_epoch;
-        if (ctrl != nullptr) {
-            e = ld_u32_v(ctrl) + 1;
-            if (e == 0) e = 1;
-        }
+        if (ctrl != nullptr) e = take_ticket(ctrl);
         s_epoch = e;
     }
     __syncthreads();
@@ -332,28 +342,13 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
             unpack_results<DT>(a, count, nbytes, 0, npk, rot == ng ? 0 : rot, j, j + 1, epoch, max_spins, status,
                                out16, tid, stride);
     }
-    if (ctrl != nullptr) {
-        // Every block read ctrl[0] before arriving (the add releases that read
-        // and acquires the earlier arrivals); the last block to arrive
-        // publishes the epoch and resets the arrival count for the next launch,
-        // which reads it only after this launch has completed.
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t total = gridDim.x * gridDim.y;
-            uint32_t prev;
-            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctrl + 1) : "memory");
-            if (prev == total - 1) {
-                ctrl[1] = 0;
-                ctrl[0] = epoch;
-            }
-        }
-    }
+
 }
 
 inline unsigned div_up(size_t a, size_t b) { return static_cast<unsigned>((a + b - 1) / b); }
 
 template <int DT, int NR, int WB>
-cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint32_t* ctrl,
+cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
                           uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
     const size_t nbytes = count * Elem<DT>::kSize;
     const size_t npk = (nbytes + 3) / 4;
@@ -386,13 +381,14 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
     const size_t cap = static_cast<size_t>(blocks) / nranks;
     if (cap == 0) return cudaErrorCooperativeLaunchTooLarge;
     const unsigned gx = static_cast<unsigned>(std::max<size_t>(1, std::min(want, cap)));
+    if (static_cast<uint64_t>(gx) * nranks > (uint64_t(1) << kTicketBits)) return cudaErrorInvalidConfiguration;
     LLArgs args = a;
     int n_rt = nranks;
     size_t cnt = count, nb = nbytes, cq = chunk;
     bool p32 = true;
     for (int r = 0; r < nranks; ++r) p32 = p32 && reinterpret_cast<uintptr_t>(a.pkts[r]) % 32 == 0;
     uint32_t ep = epoch;
-    uint32_t* ct = ctrl;
+    uint64_t* ct = ctrl;
     uint64_t ms = max_spins;
     int32_t* st = status;
     bool i16 = in16, o16 = out16;
@@ -416,7 +412,7 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
 }
 
 template <int DT, int WB>
-cudaError_t coop_ranks(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint32_t* ctrl,
+cudaError_t coop_ranks(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
                        uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
     switch (nranks) {
     case 1: return coop_dispatch<DT, 1, WB>(1, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
@@ -433,7 +429,7 @@ cudaError_t coop_ranks(int nranks, const LLArgs& a, size_t count, uint32_t epoch
 
 template <int WB>
 cudaError_t coop_launch(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, void* res, size_t count,
-                        uint32_t epoch, uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16,
+                        uint32_t epoch, uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16,
                         cudaStream_t stream) {
     LLArgs a;
     a.data = data;

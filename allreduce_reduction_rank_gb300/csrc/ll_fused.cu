@@ -6,7 +6,7 @@
 namespace sar {
 
 cudaError_t launch_ll_fused(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, size_t count,
-                            uint32_t epoch, uint32_t* ctrl, uint64_t max_spins, int32_t* status, bool in16,
+                            uint32_t epoch, uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16,
                             bool out16, cudaStream_t stream) {
     return llc::coop_launch<llc::kDirect>(dt, nranks, data, pkts, nullptr, count, epoch, ctrl, max_spins, status,
                                           in16, out16, stream);

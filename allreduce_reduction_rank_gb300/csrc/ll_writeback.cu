@@ -6,7 +6,7 @@
 namespace sar {
 
 cudaError_t launch_ll_writeback(sar_dtype dt, int nranks, const RankPtrs& data, void* const* pkts, void* res,
-                                size_t count, uint32_t epoch, uint32_t* ctrl, bool multi_dest, uint64_t max_spins,
+                                size_t count, uint32_t epoch, uint64_t* ctrl, bool multi_dest, uint64_t max_spins,
                                 int32_t* status, bool in16, bool out16, cudaStream_t stream) {
     if (multi_dest)
         return llc::coop_launch<llc::kPacketsAll>(dt, nranks, data, pkts, res, count, epoch, ctrl, max_spins, status,

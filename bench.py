@@ -343,7 +343,7 @@ def ll_fused_row(torch, sar, wl, dev, stream, calls):
     pk = [torch.zeros(sar.sar_ll_packet_bytes(wl.count, wl.dtype), dtype=torch.uint8, device=dev)
           for _ in range(wl.nranks)]
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    ctrl = torch.zeros(2, dtype=torch.int32, device=dev)
+    ctrl = torch.zeros(1, dtype=torch.int64, device=dev)
     pi, po, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in dout], [t.data_ptr() for t in pk]
     epoch = [0]
 
@@ -359,7 +359,7 @@ def ll_fused_row(torch, sar, wl, dev, stream, calls):
     with torch.cuda.stream(stream):
         ms = time_calls(torch, host_epoch_call, calls, stream)
         # continue the epoch sequence on the device after the host epochs
-        ctrl[0] = epoch[0]
+        sar.ll_set_device_epoch(ctrl, epoch[0])
         g_ms = time_graph(torch, device_epoch_call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
     want = rsag_result(torch, sar, din, wl, stream)
@@ -367,7 +367,7 @@ def ll_fused_row(torch, sar, wl, dev, stream, calls):
     return {"workload": wl.name + "_fused", "calls": calls, "us_per_call": round(ms * 1e3, 3),
             "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
             "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
-            "epochs_on_device": int(ctrl[0].item()), "status_ok": ok, "outputs_ok": same}
+            "epochs_on_device": sar.ll_device_epoch(ctrl), "status_ok": ok, "outputs_ok": same}
 
 
 def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
@@ -380,7 +380,7 @@ def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
     pk = [torch.zeros(nbp, dtype=torch.uint8, device=dev) for _ in range(wl.nranks)]
     res = torch.zeros(nbp, dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    ctrl = torch.zeros(2, dtype=torch.int32, device=dev)
+    ctrl = torch.zeros(1, dtype=torch.int64, device=dev)
     pi, po, pp = [t.data_ptr() for t in din], [t.data_ptr() for t in dout], [t.data_ptr() for t in pk]
     epoch = [0]
 
@@ -396,7 +396,7 @@ def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
 
     with torch.cuda.stream(stream):
         ms = time_calls(torch, host_epoch_call, calls, stream)
-        ctrl[0] = epoch[0]
+        sar.ll_set_device_epoch(ctrl, epoch[0])
         g_ms = time_graph(torch, device_epoch_call, calls, stream)
     ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
     want = rsag_result(torch, sar, din, wl, stream)

@@ -111,7 +111,7 @@ def test_device_epoch_advances_per_launch_and_per_graph_replay(sar):
         want = oracle.allreduce(ins, dt)[0]
         for g in gout:
             assert_same(g.codes(dt), want, dt, f"epoch {epoch}")
-        assert ctrl.cpu().tolist() == [epoch, 0]
+        assert sar.ll_device_epoch(ctrl) == epoch
         assert np.array_equal(pk[3].bytes(), oracle.ll_pack(ins, dt, epoch)[3])
 
     for e in (1, 2, 3):
@@ -151,8 +151,10 @@ def test_thousand_fused_calls(sar, wl):
     assert sar.sar_read_device_status(st) == sar.SAR_OK
 
 
-def test_device_epoch_wraps_past_zero(sar):
-    """The device counter at 2^32 - 1: the next epoch skips the reserved 0."""
+@pytest.mark.parametrize("last,next_epoch", [(0xFFFFFFFE, 0xFFFFFFFF), (0xFFFFFFFF, 1)])
+def test_device_epoch_wraps_past_zero(sar, last, next_epoch):
+    """After epoch 2^32 - 1 the counter's next epoch is 1: the reserved 0 is
+    skipped."""
     n, count, dt = 4, 3001, "fp32"
     rng = np.random.default_rng(12)
     ins = [random_codes(rng, dt, count) for _ in range(n)]
@@ -161,11 +163,13 @@ def test_device_epoch_wraps_past_zero(sar):
     gout = [Guarded(count * 4) for _ in range(n)]
     pk = _packets(sar, n, count, dt)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ctrl = torch.tensor([-1, 0], dtype=torch.int32, device="cuda")      # last epoch 0xFFFFFFFF
+    ctrl = torch.zeros(1, dtype=torch.int64, device="cuda")
+    sar.ll_set_device_epoch(ctrl, last)
     sar.sar_allreduce_ll_fused([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], st,
                                epoch_ctrl=ctrl, count=count, dtype=dt)
     assert sar.sar_read_device_status(st) == sar.SAR_OK
-    assert ctrl.cpu().tolist() == [1, 0]
+    assert sar.ll_device_epoch(ctrl) == next_epoch
+    assert int(ctrl.item()) & ((1 << sar.LL_EPOCH_SHIFT) - 1) == 0      # no ticket left over
     for g in gout:
         assert_same(g.codes(dt), want, dt)
-    assert np.array_equal(pk[0].bytes(), oracle.ll_pack(ins, dt, 1)[0])
+    assert np.array_equal(pk[0].bytes(), oracle.ll_pack(ins, dt, next_epoch)[0])
