@@ -8,7 +8,10 @@
 // write-back happens from registers (N*S read + N*S written); in two phases
 // the reduce-scatter writes the chunk to the owning rank's output and the
 // all-gather copies it from there to every other output: the same N*S
-// written, plus one extra S read (the reduced chunks, read back).
+// written, plus one extra S read (the reduced chunks, read back).  That read
+// is served by the L2 when the chunks fit there: the reduce-scatter stores
+// them with an evict-last policy and the all-gather reads them with
+// evict-first.
 #include "sar_device.cuh"
 #include "sar_internal.h"
 
@@ -32,7 +35,9 @@ all_gather_vec_kernel(const RankPtrs p, int n_rt, size_t nbytes, size_t chunk_by
     const uint4* src = static_cast<const uint4*>(p.out[r]);
     const size_t v = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     if (v < nfull) {
-        const uint4 x = ld_stream(src + vbase + v);
+        // The reduce-scatter stored this chunk as L2 evict-last; read it
+        // from there and let the lines go first from now on.
+        const uint4 x = ld_stream_hint(src + vbase + v, l2_policy_evict_first());
 #pragma unroll
         for (int j = 0; j < ranks<NR>(n_rt); ++j)
             if (j != r) st_stream(static_cast<uint4*>(p.out[j]) + vbase + v, x);

@@ -341,4 +341,32 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
+// L2 eviction priorities (createpolicy and the L2::cache_hint operand, sm_80
+// and later).  The reduce-scatter step stores its chunk results as
+// evict-last, so that the all-gather step that follows finds them in L2
+// instead of reading them back from HBM; the all-gather reads them as
+// evict-first, which hands those lines back to the normal eviction order.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_stream_hint(const uint4* p, uint64_t policy) {
+    uint4 v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ void st_stream_hint(uint4* p, const uint4& v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
 }  // namespace sar

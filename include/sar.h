@@ -23,10 +23,13 @@
  * Conventions shared by every entry point:
  *  - Pointer arrays (`in`, `out`, `pkts`) are HOST arrays of `nranks` DEVICE
  *    pointers.  The caller owns the arrays and every buffer.  The library
- *    copies the pointers into kernel parameters, keeps nothing after the call
- *    returns, allocates nothing and does not synchronise (except
+ *    copies the pointers into kernel parameters, keeps no caller pointer after
+ *    the call returns, allocates nothing and does not synchronise (except
  *    sar_read_device_status), so calls are stream-ordered and may be captured
- *    into a CUDA graph.
+ *    into a CUDA graph.  The only state kept between calls belongs to the LL
+ *    path on the library's fixed packet scratch (SAR_ALGO_LL_ALLPAIR and
+ *    sar_allreduce_ll_noalloc): the scratch array itself and, per device, its
+ *    address and last epoch.
  *  - `count` is the number of elements per rank.  count == 0 returns SAR_OK
  *    without launching anything.
  *  - Every argument error is returned before any launch.  nranks may be any
