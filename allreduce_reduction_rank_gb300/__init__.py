@@ -12,7 +12,7 @@ Function names follow the C ABI: :func:`sar_allreduce`,
 :func:`sar_rsag_chunk`, :func:`sar_allreduce_ll_fused`, :func:`sar_allreduce_ll_writeback`,
 :func:`sar_ll_packet_bytes`, :func:`sar_ll_pack`,
 :func:`sar_ll_unpack_reduce`, :func:`sar_allreduce_ll`, :func:`sar_allreduce_ll_double`,
-:func:`sar_allreduce_ll_noalloc`,
+:func:`sar_allreduce_ll_noalloc`, :func:`sar_allreduce_ll_cluster`,
 :func:`sar_fp8_convert`, :func:`sar_read_device_status`,
 :func:`sar_status_string`.
 """
@@ -42,6 +42,7 @@ SAR_ALGO_RSAG, SAR_ALGO_RSAG_TWO_PHASE, SAR_ALGO_LL_ALLPAIR = 0, 1, 2
  SAR_ERR_MISALIGNED, SAR_ERR_CUDA, SAR_ERR_TIMEOUT) = range(7)
 SAR_MAX_RANKS = 32
 SAR_LL_NOALLOC_SCRATCH_BYTES = 16 << 20
+SAR_LL_CLUSTER_MAX_RANKS = 16
 
 DTYPE_CODES = {"bf16": SAR_BF16, "fp16": SAR_FP16, "fp32": SAR_FP32, "e4m3fn": SAR_FP8_E4M3FN,
                "e4m3b15": SAR_FP8_E4M3B15}
@@ -67,13 +68,15 @@ lib.sar_allreduce_ll_double.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32,
 lib.sar_allreduce_ll_fused.argtypes = [_vpp, _vpp, _vpp, _i32, _sz, _i32, _u32, _vp, _u64, _vp, _vp]
 lib.sar_allreduce_ll_writeback.argtypes = [_vpp, _vpp, _vpp, _vp, _i32, _sz, _i32, _u32, _vp, _i32, _u64, _vp, _vp]
 lib.sar_allreduce_ll_noalloc.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u64, _vp, _vp]
+lib.sar_allreduce_ll_cluster.argtypes = [_vpp, _vpp, _i32, _sz, _i32, _u64, _vp, _vp]
 lib.sar_fp8_convert.argtypes = [_vp, _i32, _vp, _i32, _sz, _vp]
 lib.sar_read_device_status.argtypes = [_vp, _vp]
 lib.sar_status_string.argtypes = [_i32]
 lib.sar_status_string.restype = ctypes.c_char_p
 for _f in ("sar_allreduce", "sar_allreduce_accum", "sar_allreduce_ll_fused", "sar_allreduce_ll_writeback",
            "sar_reduce_scatter", "sar_all_gather", "sar_ll_pack", "sar_ll_unpack_reduce",
-           "sar_allreduce_ll", "sar_allreduce_ll_double", "sar_allreduce_ll_noalloc", "sar_fp8_convert",
+           "sar_allreduce_ll", "sar_allreduce_ll_double", "sar_allreduce_ll_noalloc", "sar_allreduce_ll_cluster",
+           "sar_fp8_convert",
            "sar_read_device_status"):
     getattr(lib, _f).restype = _i32
 
@@ -263,6 +266,16 @@ def sar_allreduce_ll_noalloc(ins, outs, status=None, max_spins: int = 1 << 20, c
     pout, _ = _ptrs(outs)
     _check(lib.sar_allreduce_ll_noalloc(pin, pout, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), max_spins,
                                         None if status is None else _addr(status), _stream(stream)))
+
+
+def sar_allreduce_ll_cluster(ins, outs, status, max_spins: int = 1 << 20, count=None, dtype=None,
+                             stream=None) -> None:
+    """LL allreduce with the packets exchanged through the shared memory of
+    thread-block clusters (one CTA per simulated rank; at most 16 ranks)."""
+    pin, n = _ptrs(ins)
+    pout, _ = _ptrs(outs)
+    _check(lib.sar_allreduce_ll_cluster(pin, pout, n, _count(count, ins[0]), _dtype_code(dtype, ins[0]), max_spins,
+                                        _addr(status), _stream(stream)))
 
 
 # The device epoch counter of sar_allreduce_ll_fused / _writeback: one uint64,

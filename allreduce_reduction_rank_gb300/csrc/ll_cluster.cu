@@ -1,0 +1,268 @@
+// ll_cluster.cu -- the LL all-pair allreduce through distributed shared
+// memory: the simulated ranks of one slice of the data are the CTAs of one
+// thread-block cluster.
+//
+// mscclpp commit history, the allreduce_allpair_packet fix: each rank sends
+// its data as flag-checked LL packets into every peer's scratch, the peer
+// polls the flags in its own scratch, reduces and writes the result back,
+// all in the same thread block.  On one GB300 the peers of a slice are the N
+// CTAs of a cluster (CTA rank r = simulated rank r), and a CTA's scratch is
+// its shared memory, which the other CTAs of the cluster write directly
+// (st.shared::cluster to a mapa-translated address):
+//
+//   zero   : every CTA clears its packet slots (N x kSlots 8-byte packets),
+//            then the cluster synchronises once, so no slot is written before
+//            its owner has cleared it;
+//   send   : CTA k turns its input words for the slice of every chunk r into
+//            packets {payload, flag} and stores them into CTA r's slots
+//            [k][0..kSlots) (16-byte stores of two packets, each packet a
+//            single-copy-atomic 8-byte element);
+//   reduce : thread t of CTA r polls slot [k][t] for every k until its flag is
+//            set (bounded; a timeout is recorded in the status word), adds the
+//            payloads in rank order 0..N-1 in binary32, rounds once and writes
+//            the result word to all N outputs;
+//   exit   : the cluster synchronises again, so no CTA leaves while another
+//            may still write into its shared memory.
+//
+// The slots start every launch at zero ("never written"), so every launch
+// uses the flag value 1: no epoch is carried between launches and a CUDA
+// graph can replay the call as it is.  Packets never touch global memory:
+// HBM traffic is N*S read plus N*S written, as for the rsag kernel.  Clusters
+// hold at most 16 CTAs (8 portably), so N <= 16.
+//
+// Slice of cluster `team` in chunk r: packets [r*chunk + team*kSlots, +kSlots)
+// of the rank's packet range (chunk = packets per rank chunk, a multiple of
+// 4), cut at the end of the chunk and of the buffer.  Packet w holds bytes
+// 4w..4w+3 of a rank's input, zero past its end, as in sar_ll_pack.
+#include "ll_packets.cuh"
+#include "sar_device.cuh"
+#include "sar_internal.h"
+
+namespace sar {
+namespace llk {
+
+constexpr int kSlots = kThreads;          // packets per rank and slice: one per reducing thread
+constexpr int kMaxClusterRanks = SAR_LL_CLUSTER_MAX_RANKS;
+constexpr uint32_t kFlag = 1;             // flag of a written slot (cleared slots hold 0)
+constexpr uint64_t kSpinPolls = 16;       // immediate re-reads before a poll backs off
+constexpr unsigned kMaxSleepNs = 1024;
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of `local` (a shared::cta address) in CTA `rank` of
+// this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster2(uint32_t addr, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.cluster.shared::cluster.v2.u64 [%0], {%1, %2};" :: "r"(addr), "l"(a), "l"(b)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster1(uint32_t addr, uint64_t a) {
+    asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" :: "r"(addr), "l"(a) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_slot(uint32_t addr) {
+    uint64_t v;
+    asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
+    int32_t v;
+    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t packet(uint32_t payload) {
+    return static_cast<uint64_t>(payload) | (static_cast<uint64_t>(kFlag) << 32);
+}
+
+// Payload word w of a byte buffer of nbytes, zero past the end.
+__device__ __forceinline__ uint32_t word_bytes(const unsigned char* b, size_t nbytes, size_t w) {
+    uint32_t v = 0;
+    for (int k = 0; k < 4; ++k)
+        if (4 * w + k < nbytes) v |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
+    return v;
+}
+
+template <int DT, int NR>
+__global__ void __launch_bounds__(kThreads)
+cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk, uint64_t max_spins,
+               int32_t* status, bool in16, bool out16) {
+    extern __shared__ __align__(16) uint64_t slots[];   // [sender k][kSlots]
+    constexpr int EP = PerWord<DT>::kN;
+    constexpr int WIN = NR > 0 ? NR : 16;
+    const int n = ranks<NR>(n_rt);
+    const uint32_t me = blockIdx.x % static_cast<uint32_t>(n);      // CTA rank in the cluster = simulated rank
+    const size_t team = blockIdx.x / static_cast<uint32_t>(n);
+    const size_t npk = (nbytes + 3) / 4;
+    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(slots));
+
+    // zero: no global memory is touched yet, so this overlaps the previous
+    // kernel's drain (programmatic launch).
+    for (int i = threadIdx.x; i < n * kSlots; i += kThreads) slots[i] = 0;
+    cluster_sync();
+    pdl_wait();
+
+    // send: 4 packets (one 16-byte input vector) per item; item v covers
+    // destination r = v / (kSlots/4), packets 4*(v % (kSlots/4)) .. +3 of the slice.
+    const unsigned char* src = static_cast<const unsigned char*>(p.in[me]);
+    constexpr int kGroups = kSlots / 4;
+    for (int v = threadIdx.x; v < n * kGroups; v += kThreads) {
+        const int r = v / kGroups, g = v % kGroups;
+        const size_t lo = static_cast<size_t>(r) * chunk;
+        const size_t end = min(npk, lo + chunk);
+        const size_t w = lo + team * kSlots + 4 * static_cast<size_t>(g);
+        if (w >= end) continue;
+        uint32_t x[4];
+        if (in16 && 4 * (w + 4) <= nbytes) {
+            const uint4 q = ld_stream(reinterpret_cast<const uint4*>(src) + w / 4);
+            x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+        } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) x[m] = w + m < end ? word_bytes(src, nbytes, w + m) : 0;
+        }
+        const uint32_t dst = map_to_rank(base + static_cast<uint32_t>((me * kSlots + 4 * g) * 8), r);
+        if (w + 4 <= end) {
+            st_cluster2(dst, packet(x[0]), packet(x[1]));
+            st_cluster2(dst + 16, packet(x[2]), packet(x[3]));
+        } else {
+            for (int m = 0; m < 4 && w + m < end; ++m) st_cluster1(dst + 8 * m, packet(x[m]));
+        }
+    }
+
+    // reduce: thread t owns packet w of this CTA's chunk slice.
+    const size_t lo = static_cast<size_t>(me) * chunk;
+    const size_t end = min(npk, lo + chunk);
+    const size_t w = lo + team * kSlots + threadIdx.x;
+    if (w < end) {
+        uint64_t pk[WIN];
+        const uint32_t mine = base + static_cast<uint32_t>(threadIdx.x * 8);
+#pragma unroll
+        for (int k = 0; k < WIN; ++k)
+            if (NR > 0 || k < n) pk[k] = ld_slot(mine + static_cast<uint32_t>(k * kSlots * 8));
+        unsigned ns = 32;
+        bool ok = true;
+        for (uint64_t spin = 0;; ++spin) {
+            bool ready = true;
+#pragma unroll
+            for (int k = 0; k < WIN; ++k)
+                if (NR > 0 || k < n) ready = ready && static_cast<uint32_t>(pk[k] >> 32) == kFlag;
+            if (ready) break;
+            if (spin >= max_spins) {
+                atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+                ok = false;
+                break;
+            }
+            if (spin >= kSpinPolls) {
+                if (ld_status_v(status) != 0) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(ns);
+                if (ns < kMaxSleepNs) ns *= 2;
+            }
+#pragma unroll
+            for (int k = 0; k < WIN; ++k)
+                if ((NR > 0 || k < n) && static_cast<uint32_t>(pk[k] >> 32) != kFlag)
+                    pk[k] = ld_slot(mine + static_cast<uint32_t>(k * kSlots * 8));
+        }
+        if (ok) {
+            float acc[EP];
+#pragma unroll
+            for (int k = 0; k < WIN; ++k) {
+                if (NR == 0 && k >= n) break;
+                float x[EP];
+                widen_word<DT>(static_cast<uint32_t>(pk[k]), x);
+#pragma unroll
+                for (int e = 0; e < EP; ++e) acc[e] = k == 0 ? x[e] : __fadd_rn(acc[e], x[e]);
+            }
+            if (out16 && 4 * (w + 1) <= nbytes) {
+                const uint32_t y = narrow_word<DT>(acc);
+#pragma unroll
+                for (int j = 0; j < WIN; ++j)
+                    if (NR > 0 || j < n) st_stream_word(static_cast<uint32_t*>(p.out[j]) + w, y);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    const size_t i = w * EP + e;
+                    if (i < count)
+                        for (int j = 0; j < n; ++j) store_elem<DT>(p.out[j], i, acc[e]);
+                }
+            }
+        }
+    }
+    // exit: every CTA of the cluster has finished writing into the others'
+    // slots before any of them leaves.
+    cluster_sync();
+}
+
+template <int DT, int NR>
+cudaError_t cluster_dispatch(int nranks, const RankPtrs& p, size_t count, uint64_t max_spins, int32_t* status,
+                             bool in16, bool out16, cudaStream_t s) {
+    const size_t nbytes = count * Elem<DT>::kSize;
+    const size_t npk = (nbytes + 3) / 4;
+    const size_t chunk = ((npk + nranks - 1) / nranks + 3) / 4 * 4;
+    const size_t teams = (chunk + kSlots - 1) / kSlots;
+    if (teams * static_cast<size_t>(nranks) > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(nranks) * kSlots * 8;
+    // Clusters above 8 CTAs are not portable: allowed explicitly.
+    if (nranks > 8) {
+        const cudaError_t e = cudaFuncSetAttribute(cluster_kernel<DT, NR>,
+                                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(nranks);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(teams * static_cast<size_t>(nranks)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, cluster_kernel<DT, NR>, p, nranks, count, nbytes, chunk, max_spins, status,
+                              in16, out16);
+}
+
+template <int DT>
+cudaError_t cluster_ranks(int nranks, const RankPtrs& p, size_t count, uint64_t max_spins, int32_t* status,
+                          bool in16, bool out16, cudaStream_t s) {
+    switch (nranks) {
+    case 1: return cluster_dispatch<DT, 1>(1, p, count, max_spins, status, in16, out16, s);
+    case 2: return cluster_dispatch<DT, 2>(2, p, count, max_spins, status, in16, out16, s);
+    case 4: return cluster_dispatch<DT, 4>(4, p, count, max_spins, status, in16, out16, s);
+    case 8: return cluster_dispatch<DT, 8>(8, p, count, max_spins, status, in16, out16, s);
+    case 16: return cluster_dispatch<DT, 16>(16, p, count, max_spins, status, in16, out16, s);
+    default:
+        if (nranks < 1 || nranks > kMaxClusterRanks) return cudaErrorInvalidValue;
+        return cluster_dispatch<DT, 0>(nranks, p, count, max_spins, status, in16, out16, s);
+    }
+}
+
+}  // namespace llk
+
+cudaError_t launch_ll_cluster(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
+                              int32_t* status, bool in16, bool out16, cudaStream_t stream) {
+    switch (dt) {
+    case SAR_BF16: return llk::cluster_ranks<SAR_BF16>(nranks, p, count, max_spins, status, in16, out16, stream);
+    case SAR_FP16: return llk::cluster_ranks<SAR_FP16>(nranks, p, count, max_spins, status, in16, out16, stream);
+    case SAR_FP32: return llk::cluster_ranks<SAR_FP32>(nranks, p, count, max_spins, status, in16, out16, stream);
+    case SAR_FP8_E4M3FN:
+        return llk::cluster_ranks<SAR_FP8_E4M3FN>(nranks, p, count, max_spins, status, in16, out16, stream);
+    case SAR_FP8_E4M3B15:
+        return llk::cluster_ranks<SAR_FP8_E4M3B15>(nranks, p, count, max_spins, status, in16, out16, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sar

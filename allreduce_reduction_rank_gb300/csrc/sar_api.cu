@@ -367,6 +367,25 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
                                          max_spins, d_status, in16, out16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+SAR_API sar_status sar_allreduce_ll_cluster(const void* const* in, void* const* out, int nranks, size_t count,
+                                            sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
+                                            sar_stream_t stream) {
+    if (nranks < 1 || nranks > SAR_LL_CLUSTER_MAX_RANKS) return SAR_ERR_UNSUPPORTED_NRANKS;
+    RankPtrs p;
+    bool vec = false, launch = false;
+    sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
+    if (st != SAR_OK) return st;
+    if ((st = check_status_args(max_spins, d_status)) != SAR_OK) return st;
+    if (!launch) return SAR_OK;
+    bool in16 = true, out16 = true;
+    for (int r = 0; r < nranks; ++r) {
+        in16 = in16 && aligned(in[r], 16);
+        out16 = out16 && aligned(out[r], 16);
+    }
+    return to_status(launch_ll_cluster(dtype, nranks, p, count, max_spins, d_status, in16, out16,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 SAR_API sar_status sar_fp8_convert(const void* src, sar_dtype src_dtype, void* dst, sar_dtype dst_dtype,
                                    size_t count, sar_stream_t stream) {
     if (!valid_dtype(src_dtype) || !valid_dtype(dst_dtype)) return SAR_ERR_UNSUPPORTED_DTYPE;

@@ -103,6 +103,11 @@ sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, i
 // returns the array's device address there (nullptr if it was not looked up).
 unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoch);
 
+// LL through distributed shared memory: one cluster of nranks CTAs per slice
+// (ll_cluster.cu); nranks <= SAR_LL_CLUSTER_MAX_RANKS.
+cudaError_t launch_ll_cluster(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
+                              int32_t* status, bool in16, bool out16, cudaStream_t stream);
+
 cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
                            size_t count, bool vec, cudaStream_t stream);
 

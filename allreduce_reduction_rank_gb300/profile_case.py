@@ -3,8 +3,8 @@
     python -m allreduce_reduction_rank_gb300.profile_case CASE NRANKS BYTES_PER_RANK DTYPE [--calls K]
 
 CASE is one of rsag, rsag_two_phase, ll_allpair (sar_allreduce with that
-algorithm), ll (sar_allreduce_ll), ll_fused, ll_writeback_multi_dest,
-ll_writeback_own_output.  The inputs are seeded normal values on the device
+algorithm), ll (sar_allreduce_ll), ll_fused, ll_cluster,
+ll_writeback_multi_dest, ll_writeback_own_output.  The inputs are seeded normal values on the device
 (their values do not matter for timing), the buffers are allocated once, and
 the case runs K times (default 3) with epochs 1..K, then synchronises and
 checks that every output equals the rsag allreduce of the same inputs.  Only
@@ -19,7 +19,7 @@ import torch
 
 import allreduce_reduction_rank_gb300 as sar
 
-CASES = ("rsag", "rsag_two_phase", "ll_allpair", "ll", "ll_fused", "ll_writeback_multi_dest",
+CASES = ("rsag", "rsag_two_phase", "ll_allpair", "ll", "ll_fused", "ll_cluster", "ll_writeback_multi_dest",
          "ll_writeback_own_output")
 STORAGE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32, "e4m3fn": torch.uint8,
            "e4m3b15": torch.uint8}
@@ -58,6 +58,8 @@ def main() -> None:
             sar.sar_allreduce_ll(ins, outs, pk, epoch, st, count=count, dtype=a.dtype)
         elif a.case == "ll_fused":
             sar.sar_allreduce_ll_fused(ins, outs, pk, st, epoch=epoch, count=count, dtype=a.dtype)
+        elif a.case == "ll_cluster":
+            sar.sar_allreduce_ll_cluster(ins, outs, st, count=count, dtype=a.dtype)
         else:
             sar.sar_allreduce_ll_writeback(ins, outs, pk, res, st, multi_dest=a.case.endswith("multi_dest"),
                                            epoch=epoch, count=count, dtype=a.dtype)

@@ -409,6 +409,31 @@ def ll_writeback_row(torch, sar, wl, dev, stream, calls, multi_dest):
             "status_ok": ok, "outputs_ok": same}
 
 
+def ll_cluster_row(torch, sar, wl, dev, stream, calls):
+    """LL through the shared memory of thread-block clusters: eager and a
+    CUDA graph of `calls` calls (no epoch or scratch, so the graph replays
+    as it is)."""
+    ins = wl.inputs()
+    din = [upload(torch, x, wl.dtype, dev) for x in ins]
+    dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pi, po = [t.data_ptr() for t in din], [t.data_ptr() for t in dout]
+
+    def call():
+        sar.sar_allreduce_ll_cluster(pi, po, st.data_ptr(), count=wl.count, dtype=wl.dtype, stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_calls(torch, call, calls, stream)
+        g_ms = time_graph(torch, call, calls, stream)
+    ok = sar.sar_read_device_status(st.data_ptr(), stream.cuda_stream) == sar.SAR_OK
+    want = rsag_result(torch, sar, din, wl, stream)
+    same = all(torch.equal(t, want) for t in dout)
+    return {"workload": wl.name + "_cluster", "calls": calls, "us_per_call": round(ms * 1e3, 3),
+            "GBps": round(wl.algo_bytes / (ms * 1e-3) / GB, 2),
+            "graph_us_per_call": round(g_ms * 1e3, 3), "graph_GBps": round(wl.algo_bytes / (g_ms * 1e-3) / GB, 2),
+            "status_ok": ok, "outputs_ok": same}
+
+
 def convert_row(torch, sar, dev, stream, count=1 << 26):
     x = torch.randn(count, dtype=torch.float32, device=dev, generator=torch.Generator(device=dev).manual_seed(0))
     y = torch.empty(count, dtype=torch.uint8, device=dev)
@@ -764,6 +789,8 @@ def run_gpu(args, d: Dist) -> None:
         plan += [(w.name, lambda w=w: ll_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_double", lambda w=w: ll_double_row(torch, sar, w, dev, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_fused", lambda w=w: ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
+        plan += [(w.name + "_cluster", lambda w=w: ll_cluster_row(torch, sar, w, dev, stream, W.LL_CALLS))
+                 for w in W.C5]
         plan += [(f"{w.name}_writeback_{'multi_dest' if m else 'own_output'}",
                   lambda w=w, m=m: ll_writeback_row(torch, sar, w, dev, stream, W.LL_CALLS, m))
                  for w in W.C5 for m in (True, False)]

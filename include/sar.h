@@ -335,6 +335,41 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
                                               uint64_t* d_epoch, int multi_dest, uint64_t max_spins,
                                               int32_t* d_status, sar_stream_t stream);
 
+/* Largest rank count of sar_allreduce_ll_cluster (CTAs per thread-block cluster). */
+#define SAR_LL_CLUSTER_MAX_RANKS 16
+
+/*
+ * sar_allreduce_ll_cluster -- the LL all-pair allreduce with the packets
+ * exchanged through distributed shared memory inside thread-block clusters
+ * (mscclpp commit history, the allreduce_allpair_packet fix: each rank sends
+ * its data as flag-checked packets into every peer's scratch, the peer polls
+ * its own scratch, reduces and writes back, all in one thread block).
+ *
+ * The packet range of every rank is cut into slices of 256 packets per rank
+ * chunk; each slice is handled by one cluster of nranks CTAs, CTA r acting
+ * for simulated rank r.  CTA k packs its input words of the slice of every
+ * chunk r into 8-byte packets {payload, flag} and stores them into the shared
+ * memory of CTA r; CTA r polls the flags of the packets it received from all
+ * ranks (bounded by max_spins re-reads per packet), adds the payloads in rank
+ * order 0..N-1 in binary32, rounds once and writes the result to all N
+ * outputs.  Results equal sar_allreduce's bit for bit.
+ *
+ * The packet slots live in each CTA's shared memory and are cleared at the
+ * start of every launch (before a cluster barrier), so the call needs no
+ * scratch buffer, no epoch and no state between calls: it allocates nothing,
+ * and a CUDA graph may replay it as it is.  Packets never reach global
+ * memory, so the HBM traffic is N*S read plus N*S written.
+ *
+ * nranks : 1 .. SAR_LL_CLUSTER_MAX_RANKS (16; clusters of more than 8 CTAs use
+ *          the non-portable cluster size), else SAR_ERR_UNSUPPORTED_NRANKS.
+ * in, out, count, dtype : as sar_allreduce (in place allowed).
+ * max_spins, d_status : as sar_ll_unpack_reduce; a poll can run out only when
+ *          max_spins is smaller than the time the peers' stores take.
+ */
+SAR_API sar_status sar_allreduce_ll_cluster(const void* const* in, void* const* out, int nranks, size_t count,
+                                            sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
+                                            sar_stream_t stream);
+
 /*
  * Size of the fixed LL packet scratch inside the library used by
  * sar_allreduce_ll_noalloc: 16 MiB per GPU.  A call fits when
