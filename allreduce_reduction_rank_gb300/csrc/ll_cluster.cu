@@ -10,9 +10,10 @@
 // its shared memory, which the other CTAs of the cluster write directly
 // (st.shared::cluster to a mapa-translated address):
 //
-//   zero   : every CTA clears its packet slots (N x kSlots 8-byte packets),
-//            then the cluster synchronises once, so no slot is written before
-//            its owner has cleared it;
+//   clear  : every CTA clears its packet slots (N x kSlots 8-byte packets)
+//            and arrives at a cluster barrier; it loads its input words and
+//            waits at the barrier before its first store into another CTA,
+//            so no slot is written before its owner has cleared it;
 //   send   : CTA k turns its input words for the slice of every chunk r into
 //            packets {payload, flag} and stores them into CTA r's slots
 //            [k][0..kSlots) (16-byte stores of two packets, each packet a
@@ -21,8 +22,9 @@
 //            set (bounded; a timeout is recorded in the status word), adds the
 //            payloads in rank order 0..N-1 in binary32, rounds once and writes
 //            the result word to all N outputs;
-//   exit   : the cluster synchronises again, so no CTA leaves while another
-//            may still write into its shared memory.
+//   exit   : every CTA arrives at a second cluster barrier after its last
+//            store into another CTA and waits there before it leaves, so no
+//            CTA leaves while another may still write into its shared memory.
 //
 // The slots start every launch at zero ("never written"), so every launch
 // uses the flag value 1: no epoch is carried between launches and a CUDA
@@ -47,8 +49,15 @@ constexpr uint32_t kFlag = 1;             // flag of a written slot (cleared slo
 constexpr uint64_t kSpinPolls = 16;       // immediate re-reads before a poll backs off
 constexpr unsigned kMaxSleepNs = 1024;
 
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The two halves of a cluster barrier.  Arrive publishes this CTA's earlier
+// memory operations (release); wait returns once every CTA of the cluster has
+// arrived and makes theirs visible (acquire).  Work placed between the halves
+// hides the barrier's latency.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Shared-memory address of `local` (a shared::cta address) in CTA `rank` of
@@ -102,38 +111,57 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     const size_t npk = (nbytes + 3) / 4;
     const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(slots));
 
-    // zero: no global memory is touched yet, so this overlaps the previous
-    // kernel's drain (programmatic launch).
+    // clear: no global memory is touched yet, so this overlaps the previous
+    // kernel's drain (programmatic launch).  The barrier's wait comes only
+    // before the first store into another CTA's slots.
     for (int i = threadIdx.x; i < n * kSlots; i += kThreads) slots[i] = 0;
-    cluster_sync();
+    cluster_arrive();
     pdl_wait();
 
     // send: 4 packets (one 16-byte input vector) per item; item v covers
-    // destination r = v / (kSlots/4), packets 4*(v % (kSlots/4)) .. +3 of the slice.
+    // destination r = v / (kSlots/4), packets 4*(v % (kSlots/4)) .. +3 of the
+    // slice.  A thread loads all of its items, then waits for the cluster,
+    // then stores them.
     const unsigned char* src = static_cast<const unsigned char*>(p.in[me]);
     constexpr int kGroups = kSlots / 4;
-    for (int v = threadIdx.x; v < n * kGroups; v += kThreads) {
+    constexpr int kItems = ((NR > 0 ? NR : kMaxClusterRanks) * kGroups + kThreads - 1) / kThreads;
+    uint32_t x[kItems][4];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+        const int v = threadIdx.x + u * kThreads;
         const int r = v / kGroups, g = v % kGroups;
         const size_t lo = static_cast<size_t>(r) * chunk;
         const size_t end = min(npk, lo + chunk);
         const size_t w = lo + team * kSlots + 4 * static_cast<size_t>(g);
-        if (w >= end) continue;
-        uint32_t x[4];
+        x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0;
+        if (v >= n * kGroups || w >= end) continue;
         if (in16 && 4 * (w + 4) <= nbytes) {
             const uint4 q = ld_stream(reinterpret_cast<const uint4*>(src) + w / 4);
-            x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+            x[u][0] = q.x; x[u][1] = q.y; x[u][2] = q.z; x[u][3] = q.w;
         } else {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) x[m] = w + m < end ? word_bytes(src, nbytes, w + m) : 0;
-        }
-        const uint32_t dst = map_to_rank(base + static_cast<uint32_t>((me * kSlots + 4 * g) * 8), r);
-        if (w + 4 <= end) {
-            st_cluster2(dst, packet(x[0]), packet(x[1]));
-            st_cluster2(dst + 16, packet(x[2]), packet(x[3]));
-        } else {
-            for (int m = 0; m < 4 && w + m < end; ++m) st_cluster1(dst + 8 * m, packet(x[m]));
+            for (int m = 0; m < 4; ++m) x[u][m] = w + m < end ? word_bytes(src, nbytes, w + m) : 0;
         }
     }
+    cluster_wait();
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+        const int v = threadIdx.x + u * kThreads;
+        const int r = v / kGroups, g = v % kGroups;
+        const size_t lo = static_cast<size_t>(r) * chunk;
+        const size_t end = min(npk, lo + chunk);
+        const size_t w = lo + team * kSlots + 4 * static_cast<size_t>(g);
+        if (v >= n * kGroups || w >= end) continue;
+        const uint32_t dst = map_to_rank(base + static_cast<uint32_t>((me * kSlots + 4 * g) * 8), r);
+        if (w + 4 <= end) {
+            st_cluster2(dst, packet(x[u][0]), packet(x[u][1]));
+            st_cluster2(dst + 16, packet(x[u][2]), packet(x[u][3]));
+        } else {
+            for (int m = 0; m < 4 && w + m < end; ++m) st_cluster1(dst + 8 * m, packet(x[u][m]));
+        }
+    }
+    // Every packet of this CTA is stored; the matching wait comes at the exit.
+    cluster_arrive();
 
     // reduce: thread t owns packet w of this CTA's chunk slice.
     const size_t lo = static_cast<size_t>(me) * chunk;
@@ -198,7 +226,7 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     }
     // exit: every CTA of the cluster has finished writing into the others'
     // slots before any of them leaves.
-    cluster_sync();
+    cluster_wait();
 }
 
 template <int DT, int NR>
