@@ -10,13 +10,13 @@
 // its shared memory, which the other CTAs of the cluster write directly
 // (st.shared::cluster to a mapa-translated address):
 //
-//   clear  : every CTA clears its packet slots (N x kSlots 8-byte packets)
+//   clear  : every CTA clears its packet slots (N x CT 8-byte packets)
 //            and arrives at a cluster barrier; it loads its input words and
 //            waits at the barrier before its first store into another CTA,
 //            so no slot is written before its owner has cleared it;
 //   send   : CTA k turns its input words for the slice of every chunk r into
 //            packets {payload, flag} and stores them into CTA r's slots
-//            [k][0..kSlots) (16-byte stores of two packets, each packet a
+//            [k][0..CT) (16-byte stores of two packets, each packet a
 //            single-copy-atomic 8-byte element);
 //   reduce : thread t of CTA r polls slot [k][t] for every k until its flag is
 //            set (bounded; a timeout is recorded in the status word), adds the
@@ -32,7 +32,7 @@
 // HBM traffic is N*S read plus N*S written, as for the rsag kernel.  Clusters
 // hold at most 16 CTAs (8 portably), so N <= 16.
 //
-// Slice of cluster `team` in chunk r: packets [r*chunk + team*kSlots, +kSlots)
+// Slice of cluster `team` in chunk r: packets [r*chunk + team*CT, +CT)
 // of the rank's packet range (chunk = packets per rank chunk, a multiple of
 // 4), cut at the end of the chunk and of the buffer.  Packet w holds bytes
 // 4w..4w+3 of a rank's input, zero past its end, as in sar_ll_pack.
@@ -43,7 +43,6 @@
 namespace sar {
 namespace llk {
 
-constexpr int kSlots = kThreads;          // packets per rank and slice: one per reducing thread
 constexpr int kMaxClusterRanks = SAR_LL_CLUSTER_MAX_RANKS;
 constexpr uint32_t kFlag = 1;             // flag of a written slot (cleared slots hold 0)
 constexpr uint64_t kSpinPolls = 16;       // immediate re-reads before a poll backs off
@@ -98,11 +97,13 @@ __device__ __forceinline__ uint32_t word_bytes(const unsigned char* b, size_t nb
     return v;
 }
 
-template <int DT, int NR>
-__global__ void __launch_bounds__(kThreads)
+// CT: threads per CTA, also the packets per rank of a slice (one per
+// reducing thread).
+template <int DT, int NR, int CT>
+__global__ void __launch_bounds__(CT)
 cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t chunk, uint64_t max_spins,
                int32_t* status, bool in16, bool out16) {
-    extern __shared__ __align__(16) uint64_t slots[];   // [sender k][kSlots]
+    extern __shared__ __align__(16) uint64_t slots[];   // [sender k][CT]
     constexpr int EP = PerWord<DT>::kN;
     constexpr int WIN = NR > 0 ? NR : 16;
     const int n = ranks<NR>(n_rt);
@@ -114,25 +115,25 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     // clear: no global memory is touched yet, so this overlaps the previous
     // kernel's drain (programmatic launch).  The barrier's wait comes only
     // before the first store into another CTA's slots.
-    for (int i = threadIdx.x; i < n * kSlots; i += kThreads) slots[i] = 0;
+    for (int i = threadIdx.x; i < n * CT; i += CT) slots[i] = 0;
     cluster_arrive();
     pdl_wait();
 
     // send: 4 packets (one 16-byte input vector) per item; item v covers
-    // destination r = v / (kSlots/4), packets 4*(v % (kSlots/4)) .. +3 of the
+    // destination r = v / (CT/4), packets 4*(v % (CT/4)) .. +3 of the
     // slice.  A thread loads all of its items, then waits for the cluster,
     // then stores them.
     const unsigned char* src = static_cast<const unsigned char*>(p.in[me]);
-    constexpr int kGroups = kSlots / 4;
-    constexpr int kItems = ((NR > 0 ? NR : kMaxClusterRanks) * kGroups + kThreads - 1) / kThreads;
+    constexpr int kGroups = CT / 4;
+    constexpr int kItems = ((NR > 0 ? NR : kMaxClusterRanks) * kGroups + CT - 1) / CT;
     uint32_t x[kItems][4];
 #pragma unroll
     for (int u = 0; u < kItems; ++u) {
-        const int v = threadIdx.x + u * kThreads;
+        const int v = threadIdx.x + u * CT;
         const int r = v / kGroups, g = v % kGroups;
         const size_t lo = static_cast<size_t>(r) * chunk;
         const size_t end = min(npk, lo + chunk);
-        const size_t w = lo + team * kSlots + 4 * static_cast<size_t>(g);
+        const size_t w = lo + team * CT + 4 * static_cast<size_t>(g);
         x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0;
         if (v >= n * kGroups || w >= end) continue;
         if (in16 && 4 * (w + 4) <= nbytes) {
@@ -146,13 +147,13 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     cluster_wait();
 #pragma unroll
     for (int u = 0; u < kItems; ++u) {
-        const int v = threadIdx.x + u * kThreads;
+        const int v = threadIdx.x + u * CT;
         const int r = v / kGroups, g = v % kGroups;
         const size_t lo = static_cast<size_t>(r) * chunk;
         const size_t end = min(npk, lo + chunk);
-        const size_t w = lo + team * kSlots + 4 * static_cast<size_t>(g);
+        const size_t w = lo + team * CT + 4 * static_cast<size_t>(g);
         if (v >= n * kGroups || w >= end) continue;
-        const uint32_t dst = map_to_rank(base + static_cast<uint32_t>((me * kSlots + 4 * g) * 8), r);
+        const uint32_t dst = map_to_rank(base + static_cast<uint32_t>((me * CT + 4 * g) * 8), r);
         if (w + 4 <= end) {
             st_cluster2(dst, packet(x[u][0]), packet(x[u][1]));
             st_cluster2(dst + 16, packet(x[u][2]), packet(x[u][3]));
@@ -166,13 +167,13 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     // reduce: thread t owns packet w of this CTA's chunk slice.
     const size_t lo = static_cast<size_t>(me) * chunk;
     const size_t end = min(npk, lo + chunk);
-    const size_t w = lo + team * kSlots + threadIdx.x;
+    const size_t w = lo + team * CT + threadIdx.x;
     if (w < end) {
         uint64_t pk[WIN];
         const uint32_t mine = base + static_cast<uint32_t>(threadIdx.x * 8);
 #pragma unroll
         for (int k = 0; k < WIN; ++k)
-            if (NR > 0 || k < n) pk[k] = ld_slot(mine + static_cast<uint32_t>(k * kSlots * 8));
+            if (NR > 0 || k < n) pk[k] = ld_slot(mine + static_cast<uint32_t>(k * CT * 8));
         unsigned ns = 32;
         bool ok = true;
         for (uint64_t spin = 0;; ++spin) {
@@ -182,12 +183,12 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
                 if (NR > 0 || k < n) ready = ready && static_cast<uint32_t>(pk[k] >> 32) == kFlag;
             if (ready) break;
             if (spin >= max_spins) {
-                atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+                if (status != nullptr) atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
                 ok = false;
                 break;
             }
             if (spin >= kSpinPolls) {
-                if (ld_status_v(status) != 0) {
+                if (status != nullptr && ld_status_v(status) != 0) {
                     ok = false;
                     break;
                 }
@@ -197,7 +198,7 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
 #pragma unroll
             for (int k = 0; k < WIN; ++k)
                 if ((NR > 0 || k < n) && static_cast<uint32_t>(pk[k] >> 32) != kFlag)
-                    pk[k] = ld_slot(mine + static_cast<uint32_t>(k * kSlots * 8));
+                    pk[k] = ld_slot(mine + static_cast<uint32_t>(k * CT * 8));
         }
         if (ok) {
             float acc[EP];
@@ -229,18 +230,15 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
     cluster_wait();
 }
 
-template <int DT, int NR>
-cudaError_t cluster_dispatch(int nranks, const RankPtrs& p, size_t count, uint64_t max_spins, int32_t* status,
-                             bool in16, bool out16, cudaStream_t s) {
-    const size_t nbytes = count * Elem<DT>::kSize;
-    const size_t npk = (nbytes + 3) / 4;
-    const size_t chunk = ((npk + nranks - 1) / nranks + 3) / 4 * 4;
-    const size_t teams = (chunk + kSlots - 1) / kSlots;
+template <int DT, int NR, int CT>
+cudaError_t cluster_launch(int nranks, const RankPtrs& p, size_t count, size_t nbytes, size_t chunk,
+                           uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
+    const size_t teams = (chunk + CT - 1) / CT;
     if (teams * static_cast<size_t>(nranks) > 0x7FFFFFFFull) return cudaErrorInvalidValue;
-    const size_t smem = static_cast<size_t>(nranks) * kSlots * 8;
+    const size_t smem = static_cast<size_t>(nranks) * CT * 8;
     // Clusters above 8 CTAs are not portable: allowed explicitly.
     if (nranks > 8) {
-        const cudaError_t e = cudaFuncSetAttribute(cluster_kernel<DT, NR>,
+        const cudaError_t e = cudaFuncSetAttribute(cluster_kernel<DT, NR, CT>,
                                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
@@ -253,13 +251,35 @@ cudaError_t cluster_dispatch(int nranks, const RankPtrs& p, size_t count, uint64
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(teams * static_cast<size_t>(nranks)));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(CT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, cluster_kernel<DT, NR>, p, nranks, count, nbytes, chunk, max_spins, status,
+    return cudaLaunchKernelEx(&cfg, cluster_kernel<DT, NR, CT>, p, nranks, count, nbytes, chunk, max_spins, status,
                               in16, out16);
+}
+
+// Slice size (= threads per CTA): the smallest of 64, 128 and 256 packets
+// per rank that keeps the grid within 128 CTAs for 64 and within 512 CTAs for
+// 128.  Smaller slices put more CTAs, on more SMs, to work on small calls;
+// larger ones keep large calls within the clusters that fit at once.
+// Measured (graph, 8 ranks fp32, us per call for CTAs of 64 / 128 / 256
+// threads): 4 KiB 1.89 / 2.05 / 2.30, 16 KiB 1.96 / 2.08 / 2.55, 64 KiB
+// 2.35 / 2.28 / 2.54, 256 KiB 4.60 / 3.91 / 4.34, 1 MiB 15.8 / 11.3 / 11.4;
+// 16 ranks, 16 KiB 2.72 / 3.26 / 4.52, 64 KiB 4.45 / 4.36 / 4.74.
+template <int DT, int NR>
+cudaError_t cluster_dispatch(int nranks, const RankPtrs& p, size_t count, uint64_t max_spins, int32_t* status,
+                             bool in16, bool out16, cudaStream_t s) {
+    const size_t nbytes = count * Elem<DT>::kSize;
+    const size_t npk = (nbytes + 3) / 4;
+    const size_t chunk = ((npk + nranks - 1) / nranks + 3) / 4 * 4;
+    const size_t n = static_cast<size_t>(nranks);
+    if ((chunk + 63) / 64 * n <= 128)
+        return cluster_launch<DT, NR, 64>(nranks, p, count, nbytes, chunk, max_spins, status, in16, out16, s);
+    if ((chunk + 127) / 128 * n <= 512)
+        return cluster_launch<DT, NR, 128>(nranks, p, count, nbytes, chunk, max_spins, status, in16, out16, s);
+    return cluster_launch<DT, NR, 256>(nranks, p, count, nbytes, chunk, max_spins, status, in16, out16, s);
 }
 
 template <int DT>

@@ -225,7 +225,7 @@ def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, gr
             call()
         eager = time_calls(torch, call, calls, stream)
         g = time_graph(torch, call, calls, stream) if graph else None
-    name = ["rsag", "rsag_two_phase"][algo] if accum is None else f"rsag, {accum} accumulation"
+    name = ["rsag", "rsag_two_phase", "ll_allpair"][algo] if accum is None else f"rsag, {accum} accumulation"
     row = {"workload": wl.name, "algo": name, "bytes": wl.algo_bytes,
            "eager_us": round(eager * 1e3, 3), "eager_GBps": round(wl.algo_bytes / (eager * 1e-3) / GB, 1),
            "l2_resident": wl.algo_bytes <= l2_bytes}
@@ -787,6 +787,8 @@ def run_gpu(args, d: Dist) -> None:
                  for acc in ("e4m3fn", "fp16")]
         plan.append((W.C4_B15.name, lambda: rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes)))
         plan += [(w.name, lambda w=w: ll_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
+        plan += [(w.name + "_allpair", lambda w=w: dict(rsag_row(torch, sar, w, dev, stream, l2_bytes, algo=2),
+                                                        workload=w.name + "_allpair")) for w in W.C5]
         plan += [(w.name + "_double", lambda w=w: ll_double_row(torch, sar, w, dev, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_fused", lambda w=w: ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_cluster", lambda w=w: ll_cluster_row(torch, sar, w, dev, stream, W.LL_CALLS))

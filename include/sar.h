@@ -124,18 +124,23 @@ typedef enum {
  * then sar_all_gather.
  *
  * SAR_ALGO_LL_ALLPAIR runs the LL all-pair allreduce (mscclpp commit history,
- * the allreduce_allpair_packet fix): sar_ll_pack then sar_ll_unpack_reduce,
- * stream-ordered, on the packet scratch compiled into the library (the array
- * that sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  It
- * therefore takes only the sizes that fit that array (nranks *
- * sar_ll_packet_bytes(count, dtype) rounded up to 256 bytes per rank at most
- * SAR_LL_NOALLOC_SCRATCH_BYTES, e.g. up to 1 MiB per rank with 8 ranks);
- * larger calls return SAR_ERR_INVALID_ARG before any launch.  The first
- * LL_ALLPAIR or noalloc call on a device looks up the array's address; make
- * it before any CUDA graph capture on that device.  In stream order every
- * packet a call polls was written by the same call's pack kernel, so the
- * polls never wait.  Calls that overlap on the GPU (two streams without
- * ordering) share the array and race: their outputs are undefined.
+ * the allreduce_allpair_packet fix), in the faster of two forms for the size
+ * (both give the same bits):
+ *  - nranks <= SAR_LL_CLUSTER_MAX_RANKS and nranks * S <= 256 KiB: the
+ *    cluster form of sar_allreduce_ll_cluster (packets through shared memory,
+ *    no scratch, no state);
+ *  - otherwise sar_ll_pack then sar_ll_unpack_reduce, stream-ordered, on the
+ *    packet scratch compiled into the library (the array that
+ *    sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  That form
+ *    takes only the sizes that fit the array (nranks *
+ *    sar_ll_packet_bytes(count, dtype) rounded up to 256 bytes per rank at
+ *    most SAR_LL_NOALLOC_SCRATCH_BYTES, e.g. up to 1 MiB per rank with 8
+ *    ranks); larger calls return SAR_ERR_INVALID_ARG before any launch.  The
+ *    first such call on a device looks up the array's address; make it before
+ *    any CUDA graph capture on that device.  In stream order every packet a
+ *    call polls was written by the same call's pack kernel, so the polls never
+ *    wait.  Calls that overlap on the GPU (two streams without ordering) share
+ *    the array and race: their outputs are undefined.
  *
  * All three algorithms give the same bits.
  *

@@ -1,8 +1,9 @@
 """GPU parity of sar_allreduce with SAR_ALGO_LL_ALLPAIR: the LL all-pair
-packet allreduce behind the one allreduce entry point, on the library's fixed
-packet scratch.  Bar: bit-exact against the oracle (NaN by class), canaries
-intact, inputs unchanged; sizes beyond the fixed scratch are refused before
-any launch."""
+packet allreduce behind the one allreduce entry point, through cluster shared
+memory for small calls and on the library's fixed packet scratch for larger
+ones.  Bar: bit-exact against the oracle (NaN by class), canaries intact,
+inputs unchanged; sizes beyond the fixed scratch are refused before any
+launch."""
 import numpy as np
 import pytest
 import torch
@@ -114,6 +115,19 @@ def test_ll_allpair_in_a_cuda_graph(sar):
         want = oracle.allreduce(ins, dt)[0]
         for g in gout:
             assert_same(g.codes(dt), want, dt)
+
+
+@pytest.mark.parametrize("n,dt", [(8, "fp32"), (16, "bf16"), (2, "e4m3fn")])
+def test_ll_allpair_both_forms_at_the_size_threshold(sar, n, dt):
+    """Up to 256 KiB over all ranks the call runs the cluster form, above it
+    the two launches on the fixed scratch: both exact, on either side."""
+    per_rank = (256 << 10) // n // ESIZE[dt]
+    for count in (per_rank, per_rank + 1):
+        rng = np.random.default_rng([n, count])
+        ins = [random_codes(rng, dt, count) for _ in range(n)]
+        want = oracle.allreduce(ins, dt)[0]
+        gin, gout = _run(sar, ins, dt)
+        _check(gin, gout, ins, want, dt)
 
 
 def test_ll_allpair_rejects_sizes_beyond_the_scratch(sar):
