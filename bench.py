@@ -337,7 +337,7 @@ def ll_double_row(torch, sar, wl, dev, calls):
 def ll_fused_row(torch, sar, wl, dev, stream, calls):
     """LL in one cooperative launch: eager with host epochs 1..calls, and a
     CUDA graph of `calls` launches that take their epochs from the device
-    control block (so every replay continues the epoch sequence)."""
+    epoch counter (so every replay continues the epoch sequence)."""
     ins = wl.inputs()
     din = [upload(torch, x, wl.dtype, dev) for x in ins]
     dout = [torch.empty_like(din[0]) for _ in range(wl.nranks)]

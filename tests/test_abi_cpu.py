@@ -141,7 +141,7 @@ def test_argument_errors_before_launch(sar):
         sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_allreduce_accum(ptrs2, ptrs2, 2, 16, sar.SAR_BF16, 9, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_allreduce_accum(ptrs2, ptrs2, 2, 0, sar.SAR_FP8_E4M3FN, sar.SAR_FP8_E4M3FN, None) == sar.SAR_OK
-    # fused LL: host epoch 0 is reserved unless a device control block supplies it
+    # fused LL: host epoch 0 is reserved unless a device epoch counter supplies it
     assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_FP32, 0, None, 9, 4096, None) == \
         sar.SAR_ERR_INVALID_ARG
     assert L.sar_allreduce_ll_fused(ptrs2, ptrs2, ptrs2, 2, 16, sar.SAR_FP32, 0, 4100, 9, 4096, None) == \
