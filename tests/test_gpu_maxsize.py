@@ -82,3 +82,23 @@ def test_ll_packets_past_4_gib(sar):
     assert last[:4].view(np.float32)[0] == pats[1][(count - 1) % P]
     del din, dout, pk
     torch.cuda.empty_cache()
+
+
+def test_cluster_ll_past_2_32_elements(sar):
+    """sar_allreduce_ll_cluster with more than 2^32 elements per rank (2 ranks,
+    e4m3fn): packet indices past 2^30, slices past 2^21 clusters."""
+    n, dt, count = 2, "e4m3fn", (1 << 32) + 4099
+    pats = W.rank_inputs("normal", 8, dt, P, n, 4.0)
+    din = [_tiled(p, count, torch.uint8) for p in pats]
+    dout = [torch.empty_like(din[0]) for _ in range(n)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sar.sar_allreduce_ll_cluster(din, dout, st, count=count, dtype=dt)
+    assert sar.sar_read_device_status(st) == sar.SAR_OK
+    idx = _indices(count, n, dt, np.random.default_rng(5))
+    want = oracle.allreduce([p[idx % P] for p in pats], dt)[0]
+    tidx = torch.from_numpy(idx).cuda()
+    for j in range(n):
+        assert np.array_equal(dout[j][tidx].cpu().numpy(), want)
+        assert torch.equal(dout[j], dout[0])
+    del din, dout
+    torch.cuda.empty_cache()
