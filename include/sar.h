@@ -350,9 +350,11 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
  * its data as flag-checked packets into every peer's scratch, the peer polls
  * its own scratch, reduces and writes back, all in one thread block).
  *
- * The packet range of every rank is cut into slices of 256 packets per rank
- * chunk; each slice is handled by one cluster of nranks CTAs, CTA r acting
- * for simulated rank r.  CTA k packs its input words of the slice of every
+ * The packet range of every rank is cut into slices of 64, 128 or 256
+ * packets per rank chunk (the smallest that keeps the grid small enough: more
+ * clusters for small calls, the clusters that fit at once for large ones);
+ * each slice is handled by one cluster of nranks CTAs, CTA r acting for
+ * simulated rank r.  CTA k packs its input words of the slice of every
  * chunk r into 8-byte packets {payload, flag} and stores them into the shared
  * memory of CTA r; CTA r polls the flags of the packets it received from all
  * ranks (bounded by max_spins re-reads per packet), adds the payloads in rank
