@@ -128,7 +128,7 @@ typedef enum {
  * (both give the same bits):
  *  - nranks <= SAR_LL_CLUSTER_MAX_RANKS and nranks * S <= 256 KiB: the
  *    cluster form of sar_allreduce_ll_cluster (packets through shared memory,
- *    no scratch, no state);
+ *    no scratch, no state, so such calls may also overlap on the GPU);
  *  - otherwise sar_ll_pack then sar_ll_unpack_reduce, stream-ordered, on the
  *    packet scratch compiled into the library (the array that
  *    sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  That form
@@ -364,8 +364,9 @@ SAR_API sar_status sar_allreduce_ll_writeback(const void* const* in, void* const
  * The packet slots live in each CTA's shared memory and are cleared at the
  * start of every launch (before a cluster barrier), so the call needs no
  * scratch buffer, no epoch and no state between calls: it allocates nothing,
- * and a CUDA graph may replay it as it is.  Packets never reach global
- * memory, so the HBM traffic is N*S read plus N*S written.
+ * a CUDA graph may replay it as it is, and calls on different streams may
+ * run at the same time.  Packets never reach global memory, so the HBM
+ * traffic is N*S read plus N*S written.
  *
  * nranks : 1 .. SAR_LL_CLUSTER_MAX_RANKS (16; clusters of more than 8 CTAs use
  *          the non-portable cluster size), else SAR_ERR_UNSUPPORTED_NRANKS.

@@ -159,3 +159,33 @@ def test_cluster_argument_errors(sar):
     assert L.sar_allreduce_ll_cluster(arr, arr, 8, 16, code, 0, st.data_ptr(), None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_allreduce_ll_cluster(arr, arr, 8, 16, code, 1 << 20, None, None) == sar.SAR_ERR_INVALID_ARG
     assert L.sar_allreduce_ll_cluster(arr, arr, 8, 0, code, 1 << 20, st.data_ptr(), None) == sar.SAR_OK
+
+
+def test_cluster_calls_on_two_streams_overlap_safely(sar):
+    """The cluster form keeps no state between calls, so calls on two streams
+    without any ordering between them may run at the same time; both give
+    the oracle's outputs (sar_allreduce_ll_cluster directly, and
+    SAR_ALGO_LL_ALLPAIR at a size that takes the cluster form)."""
+    n, count, dt = 8, 4096, "fp32"
+    rng = np.random.default_rng(17)
+    cases = []
+    for s in range(2):
+        ins = [random_codes(rng, dt, count) for _ in range(n)]
+        gin = [Guarded.from_codes(c) for c in ins]
+        gout = [Guarded(count * 4) for _ in range(n)]
+        gall = [Guarded(count * 4) for _ in range(n)]
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cases.append((ins, gin, gout, gall, st, torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    for _ in range(50):
+        for ins, gin, gout, gall, st, stream in cases:
+            sar.sar_allreduce_ll_cluster([g.ptr for g in gin], [g.ptr for g in gout], st, count=count, dtype=dt,
+                                         stream=stream)
+            sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gall], count=count, dtype=dt,
+                              algo=sar.SAR_ALGO_LL_ALLPAIR, stream=stream)
+    torch.cuda.synchronize()
+    for ins, gin, gout, gall, st, stream in cases:
+        want = oracle.allreduce(ins, dt)[0]
+        assert sar.sar_read_device_status(st) == sar.SAR_OK
+        for g in gout + gall:
+            assert_same(g.codes(dt), want, dt)
