@@ -30,12 +30,6 @@ namespace {
 
 constexpr unsigned kMaxSleepNs = 1024;
 
-__device__ __forceinline__ int32_t ld_status(const int32_t* s) {
-    int32_t v;
-    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
-    return v;
-}
-
 // Wait until the packet (already loaded into w) carries `epoch`.  Returns
 // false when this thread gave up or saw another thread give up.
 __device__ __forceinline__ bool poll_one(const uint64_t* src, uint32_t epoch, uint64_t max_spins, int32_t* status,
@@ -47,7 +41,7 @@ __device__ __forceinline__ bool poll_one(const uint64_t* src, uint32_t epoch, ui
             atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
             return false;
         }
-        if (ld_status(status) != 0) return false;
+        if (ld_status_word(status) != 0) return false;
         __nanosleep(ns);
         if (ns < kMaxSleepNs) ns *= 2;
         w = ld_packet(src);

@@ -79,11 +79,6 @@ __device__ __forceinline__ uint64_t ld_slot(uint32_t addr) {
     asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
-    int32_t v;
-    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ uint64_t packet(uint32_t payload) {
     return static_cast<uint64_t>(payload) | (static_cast<uint64_t>(kFlag) << 32);
@@ -188,7 +183,7 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
                 break;
             }
             if (spin >= kSpinPolls) {
-                if (status != nullptr && ld_status_v(status) != 0) {
+                if (status != nullptr && ld_status_word(status) != 0) {
                     ok = false;
                     break;
                 }

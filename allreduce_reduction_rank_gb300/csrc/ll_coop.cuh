@@ -49,11 +49,6 @@ constexpr uint64_t kSpinPolls = 16;
 // Input vectors a send thread loads before it stores their packets.
 constexpr int kSendBatch = 4;
 
-__device__ __forceinline__ int32_t ld_status_v(const int32_t* s) {
-    int32_t v;
-    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
-    return v;
-}
 
 // Wait until packets w[0..n) (already loaded) carry `epoch`; false when this
 // thread gave up or saw another thread give up.
@@ -76,7 +71,7 @@ __device__ __forceinline__ bool poll(const uint64_t* src, uint32_t epoch, uint64
         // from the first miss).  Only a thread that has started to back off
         // looks at the shared status word.
         if (spin >= kSpinPolls) {
-            if (ld_status_v(status) != 0) return false;
+            if (ld_status_word(status) != 0) return false;
             __nanosleep(ns);
             if (ns < kMaxSleepNs) ns *= 2;
         }
@@ -111,7 +106,7 @@ __device__ __forceinline__ bool poll_window(uint64_t* const* pkts, int k0, int n
             return false;
         }
         if (spin >= kSpinPolls) {
-            if (ld_status_v(status) != 0) return false;
+            if (ld_status_word(status) != 0) return false;
             __nanosleep(ns);
             if (ns < kMaxSleepNs) ns *= 2;
         }

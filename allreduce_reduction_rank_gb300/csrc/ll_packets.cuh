@@ -35,6 +35,14 @@ __device__ __forceinline__ uint64_t make_packet(uint32_t payload, uint32_t epoch
 __device__ __forceinline__ uint32_t packet_flag(uint64_t p) { return static_cast<uint32_t>(p >> 32); }
 __device__ __forceinline__ uint32_t packet_payload(uint64_t p) { return static_cast<uint32_t>(p); }
 
+// The caller's status word, read fresh on every call (a poll that has to wait
+// checks whether another thread has already given up).
+__device__ __forceinline__ int32_t ld_status_word(const int32_t* s) {
+    int32_t v;
+    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
+    return v;
+}
+
 // One payload word of a result, stored to an output without allocating in L1.
 __device__ __forceinline__ void st_stream_word(uint32_t* p, uint32_t v) {
     asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
