@@ -41,8 +41,13 @@ bool is_fp8(int dt) { return dt == SAR_FP8_E4M3FN || dt == SAR_FP8_E4M3B15; }
 // with sleeps of up to about a microsecond between them).
 constexpr uint64_t kFixedScratchSpins = uint64_t(1) << 20;
 
-// SAR_ALGO_LL_ALLPAIR takes the cluster kernels up to this many bytes over all
-// ranks (N x S).
+// SAR_ALGO_LL_ALLPAIR takes the one-CTA kernel from 4 ranks up to
+// kCtaAllpairBytes and the cluster kernels up to kClusterAllpairBytes over all
+// ranks (N x S).  Measured against the cluster kernels (fp32, CUDA graph, us
+// per call): 8 x 1 KiB 1.42 / 1.77, 4 x 2 KiB 1.42 / 1.55, 4 x 1 KiB 1.31 /
+// 1.38, 2 x 4 KiB 1.51 / 1.43 (2 ranks stay with the clusters), 16 x 1 KiB
+// and 2 x 8 KiB slower in one CTA (one SM carries all of the call).
+constexpr size_t kCtaAllpairBytes = size_t(8) << 10;
 constexpr size_t kClusterAllpairBytes = size_t(256) << 10;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -210,14 +215,18 @@ SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype) {
 SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
                                  sar_dtype dtype, sar_algo algo, sar_stream_t stream) {
     if (algo == SAR_ALGO_LL_ALLPAIR) {
-        // Small calls: the packets go through the shared memory of thread-
-        // block clusters, the fastest LL form up to that size (8 ranks x
-        // 32 KiB, 16 x 16 KiB; measured: 8 ranks 1.7-2.3 us against 1.8-2.5 us
-        // for two launches from 1 to 64 KiB per rank).  Every packet a poll
+        // Small calls run in one launch without any scratch: every rank's
+        // packets in the shared memory of one CTA for the smallest calls,
+        // else in the shared memory of thread-block clusters up to 256 KiB
+        // over all ranks (the fastest LL forms at those sizes).  Every packet a poll
         // waits for is sent by the same launch, so no status word is needed.
         const size_t es = valid_dtype(dtype) ? esize_of(dtype) : 0;
-        if (es != 0 && nranks >= 1 && nranks <= SAR_LL_CLUSTER_MAX_RANKS && count_fits(count, es) &&
-            count * es * static_cast<size_t>(nranks) <= kClusterAllpairBytes) {
+        const bool small = es != 0 && nranks >= 1 && nranks <= SAR_MAX_RANKS && count_fits(count, es);
+        const bool cta = small && nranks >= 4 && count * es * static_cast<size_t>(nranks) <= kCtaAllpairBytes &&
+                         ll_cta_slot_bytes(nranks, count, dtype) <= kLLCtaMaxSlotBytes;
+        const bool cluster = small && nranks <= SAR_LL_CLUSTER_MAX_RANKS &&
+                             count * es * static_cast<size_t>(nranks) <= kClusterAllpairBytes;
+        if (cta || cluster) {
             RankPtrs p;
             bool vec = false, launch = false;
             const sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
@@ -227,8 +236,10 @@ SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nr
                 in16 = in16 && aligned(in[r], 16);
                 out16 = out16 && aligned(out[r], 16);
             }
-            return to_status(launch_ll_cluster(dtype, nranks, p, count, kFixedScratchSpins, nullptr, in16, out16,
-                                               reinterpret_cast<cudaStream_t>(stream)));
+            cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+            if (cta)
+                return to_status(launch_ll_cta(dtype, nranks, p, count, kFixedScratchSpins, nullptr, in16, out16, s));
+            return to_status(launch_ll_cluster(dtype, nranks, p, count, kFixedScratchSpins, nullptr, in16, out16, s));
         }
         // Larger calls: two launches on the fixed scratch in stream order, so
         // no poll ever waits; the bound only ends polls of calls that race on

@@ -108,6 +108,14 @@ unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoc
 cudaError_t launch_ll_cluster(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
                               int32_t* status, bool in16, bool out16, cudaStream_t stream);
 
+// LL of a small call inside one CTA, every rank's packets in its shared
+// memory (ll_cta.cu); the slots take ll_cta_slot_bytes(), at most
+// kLLCtaMaxSlotBytes.
+constexpr size_t kLLCtaMaxSlotBytes = size_t(64) << 10;
+size_t ll_cta_slot_bytes(int nranks, size_t count, sar_dtype dt);
+cudaError_t launch_ll_cta(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
+                          int32_t* status, bool in16, bool out16, cudaStream_t stream);
+
 cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
                            size_t count, bool vec, cudaStream_t stream);
 

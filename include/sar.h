@@ -124,11 +124,14 @@ typedef enum {
  * then sar_all_gather.
  *
  * SAR_ALGO_LL_ALLPAIR runs the LL all-pair allreduce (mscclpp commit history,
- * the allreduce_allpair_packet fix), in the faster of two forms for the size
- * (both give the same bits):
- *  - nranks <= SAR_LL_CLUSTER_MAX_RANKS and nranks * S <= 256 KiB: the
- *    cluster form of sar_allreduce_ll_cluster (packets through shared memory,
- *    no scratch, no state, so such calls may also overlap on the GPU);
+ * the allreduce_allpair_packet fix), in the fastest of three forms for the
+ * size (all give the same bits):
+ *  - nranks >= 4 and nranks * S <= 8 KiB: one CTA plays every rank, the
+ *    packets in its shared memory (no scratch, no state);
+ *  - otherwise, nranks <= SAR_LL_CLUSTER_MAX_RANKS and nranks * S <= 256 KiB:
+ *    the cluster form of sar_allreduce_ll_cluster (packets through shared
+ *    memory, no scratch, no state);
+ *    calls of these two forms may also overlap on the GPU;
  *  - otherwise sar_ll_pack then sar_ll_unpack_reduce, stream-ordered, on the
  *    packet scratch compiled into the library (the array that
  *    sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  That form

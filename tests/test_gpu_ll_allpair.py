@@ -1,7 +1,7 @@
 """GPU parity of sar_allreduce with SAR_ALGO_LL_ALLPAIR: the LL all-pair
-packet allreduce behind the one allreduce entry point, through cluster shared
-memory for small calls and on the library's fixed packet scratch for larger
-ones.  Bar: bit-exact against the oracle (NaN by class), canaries intact,
+packet allreduce behind the one allreduce entry point, in one CTA's shared
+memory for the smallest calls, through cluster shared memory for small ones
+and on the library's fixed packet scratch for larger ones.  Bar: bit-exact against the oracle (NaN by class), canaries intact,
 inputs unchanged; sizes beyond the fixed scratch are refused before any
 launch."""
 import numpy as np
@@ -52,6 +52,25 @@ def test_ll_allpair_matches_oracle(sar, dt, n, count):
     ins = [random_codes(rng, dt, count) for _ in range(n)]
     want = oracle.allreduce(ins, dt)[0]
     gin, gout = _run(sar, ins, dt)
+    _check(gin, gout, ins, want, dt)
+
+
+@pytest.mark.parametrize("n", [4, 5, 8, 16, 31])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_ll_allpair_one_cta_sizes(sar, dt, n):
+    """Calls of at most 8 KiB over all ranks, from 4 ranks up, run in one
+    CTA: ragged counts up to that size, aligned and at odd element offsets."""
+    limit = (8 << 10) // n // ESIZE[dt]
+    rng = np.random.default_rng([DTYPES.index(dt), n, 31])
+    for count in (1, 5, limit // 2 + 1, limit):
+        ins = [random_codes(rng, dt, count) for _ in range(n)]
+        want = oracle.allreduce(ins, dt)[0]
+        gin, gout = _run(sar, ins, dt)
+        _check(gin, gout, ins, want, dt)
+    count = limit - 1
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt, offsets=[ESIZE[dt] * (r % 3) for r in range(n)])
     _check(gin, gout, ins, want, dt)
 
 
@@ -117,11 +136,13 @@ def test_ll_allpair_in_a_cuda_graph(sar):
             assert_same(g.codes(dt), want, dt)
 
 
-@pytest.mark.parametrize("n,dt", [(8, "fp32"), (16, "bf16"), (2, "e4m3fn")])
-def test_ll_allpair_both_forms_at_the_size_threshold(sar, n, dt):
-    """Up to 256 KiB over all ranks the call runs the cluster form, above it
-    the two launches on the fixed scratch: both exact, on either side."""
-    per_rank = (256 << 10) // n // ESIZE[dt]
+@pytest.mark.parametrize("total", [8 << 10, 256 << 10], ids=["cta_to_cluster", "cluster_to_scratch"])
+@pytest.mark.parametrize("n,dt", [(8, "fp32"), (16, "bf16"), (2, "e4m3fn"), (32, "fp16")])
+def test_ll_allpair_forms_at_the_size_thresholds(sar, n, dt, total):
+    """Up to 8 KiB over all ranks (from 4 ranks) the call runs in one CTA, up
+    to 256 KiB in clusters (at most 16 ranks), above that as two launches on
+    the fixed scratch: exact on either side of each threshold."""
+    per_rank = total // n // ESIZE[dt]
     for count in (per_rank, per_rank + 1):
         rng = np.random.default_rng([n, count])
         ins = [random_codes(rng, dt, count) for _ in range(n)]
