@@ -787,8 +787,9 @@ def run_gpu(args, d: Dist) -> None:
                  for acc in ("e4m3fn", "fp16")]
         plan.append((W.C4_B15.name, lambda: rsag_row(torch, sar, W.C4_B15, dev, stream, l2_bytes)))
         plan += [(w.name, lambda w=w: ll_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
-        plan += [(w.name + "_allpair", lambda w=w: dict(rsag_row(torch, sar, w, dev, stream, l2_bytes, algo=2),
-                                                        workload=w.name + "_allpair")) for w in W.C5]
+        plan += [(w.name + "_allpair",
+                  lambda w=w: dict(rsag_row(torch, sar, w, dev, stream, l2_bytes, algo=2, calls=W.LL_CALLS),
+                                   workload=w.name + "_allpair")) for w in W.C5]
         plan += [(w.name + "_double", lambda w=w: ll_double_row(torch, sar, w, dev, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_fused", lambda w=w: ll_fused_row(torch, sar, w, dev, stream, W.LL_CALLS)) for w in W.C5]
         plan += [(w.name + "_cluster", lambda w=w: ll_cluster_row(torch, sar, w, dev, stream, W.LL_CALLS))
