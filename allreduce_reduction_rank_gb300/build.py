@@ -28,9 +28,8 @@ LIB = os.path.join(OUT, "libsar.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 # Slowest first, so the parallel build finishes sooner.
-SOURCES = ["rsag_e4m3b15.cu", "rsag_e4m3b15_acc.cu", "ll_writeback.cu", "ll_fused.cu", "ll_cluster.cu", "ll_cta.cu", "ll.cu",
-           "rsag_e4m3fn_acc.cu",
-           "rsag_e4m3fn.cu", "rsag_bf16_acc.cu", "rsag_fp16_acc.cu", "rsag_fp32_acc.cu", "rsag_fp16.cu",
+SOURCES = ["ll_writeback.cu", "ll_fused.cu", "ll_cluster.cu", "ll_cta.cu", "rsag_e4m3b15.cu", "rsag_e4m3b15_acc.cu",
+           "ll.cu", "rsag_e4m3fn_acc.cu", "rsag_e4m3fn.cu", "rsag_bf16_acc.cu", "rsag_fp16_acc.cu", "rsag_fp32_acc.cu", "rsag_fp16.cu",
            "rsag_bf16.cu", "rsag_fp32.cu", "convert.cu", "rsag.cu", "sar_api.cu", "noalloc.cu"]
 HEADERS = ["sar_device.cuh", "sar_internal.h", "rsag_kernels.cuh", "ll_coop.cuh", "ll_packets.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -75,10 +75,7 @@ ll_pack_vec_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
     if (blockIdx.x == 0 && threadIdx.x < 4) {
         const size_t w = 4 * nq + threadIdx.x;
         if (4 * w < nbytes) {
-            const unsigned char* bytes = static_cast<const unsigned char*>(p.in[r]);
-            uint32_t payload = 0;
-            for (int k = 0; k < 4; ++k)
-                if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(bytes[4 * w + k]) << (8 * k);
+            const uint32_t payload = payload_word(static_cast<const unsigned char*>(p.in[r]), nbytes, w);
             st_packet(dst + w, make_packet(payload, epoch));
         }
     }
@@ -94,10 +91,7 @@ ll_pack_bytes_kernel(const RankPtrs p, size_t nbytes, uint32_t epoch) {
     const size_t npk = (nbytes + 3) / 4;
     for (size_t w = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; w < npk;
          w += static_cast<size_t>(gridDim.x) * kThreads) {
-        uint32_t payload = 0;
-        for (int k = 0; k < 4; ++k)
-            if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
-        st_packet(dst + w, make_packet(payload, epoch));
+        st_packet(dst + w, make_packet(payload_word(b, nbytes, w), epoch));
     }
 }
 

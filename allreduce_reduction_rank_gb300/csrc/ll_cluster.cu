@@ -84,13 +84,6 @@ __device__ __forceinline__ uint64_t packet(uint32_t payload) {
     return static_cast<uint64_t>(payload) | (static_cast<uint64_t>(kFlag) << 32);
 }
 
-// Payload word w of a byte buffer of nbytes, zero past the end.
-__device__ __forceinline__ uint32_t word_bytes(const unsigned char* b, size_t nbytes, size_t w) {
-    uint32_t v = 0;
-    for (int k = 0; k < 4; ++k)
-        if (4 * w + k < nbytes) v |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
-    return v;
-}
 
 // CT: threads per CTA, also the packets per rank of a slice (one per
 // reducing thread).
@@ -136,7 +129,7 @@ cluster_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, size_t c
             x[u][0] = q.x; x[u][1] = q.y; x[u][2] = q.z; x[u][3] = q.w;
         } else {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) x[u][m] = w + m < end ? word_bytes(src, nbytes, w + m) : 0;
+            for (int m = 0; m < 4; ++m) x[u][m] = w + m < end ? payload_word(src, nbytes, w + m) : 0;
         }
     }
     cluster_wait();

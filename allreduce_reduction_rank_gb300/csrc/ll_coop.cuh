@@ -191,10 +191,7 @@ __device__ __forceinline__ void send(const LLArgs& a, size_t nbytes, uint32_t ep
     }
     const unsigned char* b = static_cast<const unsigned char*>(a.data.in[r]);
     for (size_t w = (in16 ? 4 * nfull : 0) + tid; w < npk; w += stride) {
-        uint32_t payload = 0;
-        for (int k = 0; k < 4; ++k)
-            if (4 * w + k < nbytes) payload |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
-        st_packet(mine + w, make_packet(payload, epoch));
+        st_packet(mine + w, make_packet(payload_word(b, nbytes, w), epoch));
     }
 }
 

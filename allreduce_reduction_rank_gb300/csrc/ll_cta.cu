@@ -50,12 +50,6 @@ __device__ __forceinline__ uint64_t ld_slot(const uint64_t* p) {
 __device__ __forceinline__ uint64_t packet(uint32_t payload) {
     return static_cast<uint64_t>(payload) | (static_cast<uint64_t>(kFlag) << 32);
 }
-__device__ __forceinline__ uint32_t word_bytes(const unsigned char* b, size_t nbytes, size_t w) {
-    uint32_t v = 0;
-    for (int k = 0; k < 4; ++k)
-        if (4 * w + k < nbytes) v |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
-    return v;
-}
 
 template <int DT, int NR>
 __global__ void __launch_bounds__(kCtaThreads)
@@ -84,7 +78,7 @@ cta_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t max
             st_slot4(row + w, packet(q.x), packet(q.y));
             st_slot4(row + w + 2, packet(q.z), packet(q.w));
         } else {
-            for (int m = 0; m < 4 && w + m < npk; ++m) st_slot(row + w + m, packet(word_bytes(src, nbytes, w + m)));
+            for (int m = 0; m < 4 && w + m < npk; ++m) st_slot(row + w + m, packet(payload_word(src, nbytes, w + m)));
         }
     }
 

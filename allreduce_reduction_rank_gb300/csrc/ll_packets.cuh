@@ -35,6 +35,15 @@ __device__ __forceinline__ uint64_t make_packet(uint32_t payload, uint32_t epoch
 __device__ __forceinline__ uint32_t packet_flag(uint64_t p) { return static_cast<uint32_t>(p >> 32); }
 __device__ __forceinline__ uint32_t packet_payload(uint64_t p) { return static_cast<uint32_t>(p); }
 
+// Payload word w of a byte buffer of nbytes: bytes 4w..4w+3, little-endian,
+// zero past the end (the padding of the last packet).
+__device__ __forceinline__ uint32_t payload_word(const unsigned char* b, size_t nbytes, size_t w) {
+    uint32_t v = 0;
+    for (int k = 0; k < 4; ++k)
+        if (4 * w + k < nbytes) v |= static_cast<uint32_t>(b[4 * w + k]) << (8 * k);
+    return v;
+}
+
 // The caller's status word, read fresh on every call (a poll that has to wait
 // checks whether another thread has already given up).
 __device__ __forceinline__ int32_t ld_status_word(const int32_t* s) {

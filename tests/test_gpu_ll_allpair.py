@@ -1,9 +1,9 @@
 """GPU parity of sar_allreduce with SAR_ALGO_LL_ALLPAIR: the LL all-pair
 packet allreduce behind the one allreduce entry point, in one CTA's shared
 memory for the smallest calls, through cluster shared memory for small ones
-and on the library's fixed packet scratch for larger ones.  Bar: bit-exact against the oracle (NaN by class), canaries intact,
-inputs unchanged; sizes beyond the fixed scratch are refused before any
-launch."""
+and on the library's fixed packet scratch for larger ones.  Bar: bit-exact
+against the oracle (NaN by class), canaries intact, inputs unchanged; sizes
+beyond the fixed scratch are refused before any launch."""
 import numpy as np
 import pytest
 import torch
