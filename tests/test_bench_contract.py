@@ -100,8 +100,9 @@ def test_gpu_arm_line():
 
 @pytest.mark.gpu
 def test_gpu_default_command_line(tmp_path):
-    """The command the round-end measurement runs, rows and CPU baseline
-    included: the last stdout line is the whole headline."""
+    """The default measurement command (`bench.py --gpus 1 --steps 20
+    --warmup 5`), rows and CPU baseline included: the last stdout line is the
+    whole headline."""
     side = tmp_path / "side.json"
     d = _line(["--gpus", "1", "--steps", "20", "--warmup", "5", "--rows-out", str(side)], timeout=1500)
     _common(d)
