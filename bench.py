@@ -474,7 +474,41 @@ def cpu_baseline(ins, wl, budget_s: float = 10.0) -> dict:
     return {"value": round(bytes_ / med / GB, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {sample} elements of each of the {wl.nranks} ranks, median of {len(runs)} runs "
                       f"({t_total:.1f} s)",
-            "us_per_call_sample": round(med * 1e6, 1), "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+            "us_per_call_sample": round(med * 1e6, 1), "host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
+            "all_cores": cpu_all_cores(ins, wl)}
+
+
+def host_threads() -> int:
+    """The cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_all_cores(ins, wl, budget_s: float = 5.0, per_thread: int = 1 << 20) -> dict:
+    """The same oracle call, unchanged, on disjoint element slices, one thread
+    per host core (the C call runs without the GIL).  Context for the
+    single-core figure, not a target: every element is still reduced on its
+    own, so the slices change nothing but who computes them."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    threads = host_threads()
+    total = min(wl.count, per_thread * threads)
+    edges = [total * t // threads for t in range(threads + 1)]
+    slices = [[x[edges[t]:edges[t + 1]] for x in ins] for t in range(threads) if edges[t + 1] > edges[t]]
+    runs, t_total = [], 0.0
+    with ThreadPoolExecutor(len(slices)) as ex:
+        while t_total < budget_s or len(runs) < 2:
+            t = time.perf_counter()
+            list(ex.map(lambda part: oracle.allreduce(part, wl.dtype), slices))
+            dt = time.perf_counter() - t
+            runs.append(dt)
+            t_total += dt
+    med = statistics.median(runs)
+    bytes_ = 2 * wl.nranks * total * W.ESIZE[wl.dtype]
+    return {"value": round(bytes_ / med / GB, 4), "cores": len(slices),
+            "sample": f"first {total} elements of each rank in {len(slices)} slices, median of {len(runs)} runs"}
 
 
 def cpu_model() -> str:

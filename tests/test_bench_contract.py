@@ -53,6 +53,19 @@ def test_reference_arm_line():
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
 
 
+def test_all_core_oracle_line_covers_disjoint_slices():
+    """The all-core CPU line calls the unchanged oracle on one slice per
+    thread; the slices it times cover the first elements of every rank once."""
+    import numpy as np
+    n = 3000
+    ins = [np.arange(n, dtype=np.float32) + r for r in range(3)]
+    wl = SimpleNamespace(name="t", nranks=3, dtype="fp32", count=n)
+    r = bench.cpu_all_cores(ins, wl, budget_s=0.0, per_thread=500)
+    cores = bench.host_threads()
+    assert r["cores"] == min(cores, n) and r["value"] > 0
+    assert r["sample"].startswith(f"first {min(n, 500 * cores)} elements of each rank in {r['cores']} slices")
+
+
 def test_warmup_below_three_is_refused():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], cwd=ROOT,
                          capture_output=True, text=True, timeout=120)
@@ -110,6 +123,7 @@ def test_gpu_default_command_line(tmp_path):
     assert d["roofline"]["frac"] > 0.8
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["all_cores"]["cores"] >= 1 and d["cpu_baseline"]["all_cores"]["value"] > 0
     s = json.loads(side.read_text())
     assert len(s["rows"]) > 50
     assert len(s["oracle_per_config"]) == len([bench.W.C1] + bench.W.C3 + [bench.W.C4, bench.W.C4_B15] + bench.W.C5)
