@@ -162,8 +162,8 @@ def sar_ll_packet_bytes(count: int, dtype) -> int:
 
 def sar_allreduce(ins, outs, count=None, dtype=None, algo=SAR_ALGO_RSAG, stream=None) -> None:
     """Allreduce: every outs[j] = R(sum over ranks 0..N-1 of ins[k]), by the
-    rsag kernels or (SAR_ALGO_LL_ALLPAIR) the LL packets on the library's
-    fixed scratch."""
+    rsag kernels or (SAR_ALGO_LL_ALLPAIR) LL packets in the shared memory of
+    the CTAs that make and poll them."""
     pin, n = _ptrs(ins)
     pout, n_out = _ptrs(outs)
     if n != n_out:

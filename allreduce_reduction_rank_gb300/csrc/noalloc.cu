@@ -70,11 +70,12 @@ bool supported(int n) { return n >= 1 && n <= SAR_MAX_RANKS; }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-}  // namespace
-
-sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
-                                      sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
-                                      bool clear_internal_status, cudaStream_t s) {
+// The LL allreduce (pack, then unpack-reduce) on the fixed scratch, with a
+// fresh epoch per call and device.  With d_status == nullptr the internal
+// status word is cleared first and used, so that a timeout of an earlier call
+// does not end this call's polls at once.
+sar_status fixed_scratch_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
+                                   sar_dtype dtype, uint64_t max_spins, int32_t* d_status, cudaStream_t s) {
     if (!supported(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;
     if (dtype < SAR_BF16 || dtype > SAR_FP8_E4M3B15) return SAR_ERR_UNSUPPORTED_DTYPE;
     if (in == nullptr || out == nullptr || max_spins == 0) return SAR_ERR_INVALID_ARG;
@@ -110,9 +111,7 @@ sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, i
     int32_t* status = d_status;
     if (status == nullptr) {
         status = reinterpret_cast<int32_t*>(base + SAR_LL_NOALLOC_SCRATCH_BYTES);
-        // The internal status word keeps the last call's value.
-        if (clear_internal_status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess)
-            return SAR_ERR_CUDA;
+        if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SAR_ERR_CUDA;
     }
 
     RankPtrs pack, unpack;
@@ -131,6 +130,8 @@ sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, i
     return SAR_OK;
 }
 
+}  // namespace
+
 unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoch) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     if (set_epoch) g_dev[dev].epoch.store(last_epoch);
@@ -142,8 +143,6 @@ unsigned char* testing_fixed_scratch(int dev, bool set_epoch, uint32_t last_epoc
 extern "C" SAR_API sar_status sar_allreduce_ll_noalloc(const void* const* in, void* const* out, int nranks,
                                                        size_t count, sar_dtype dtype, uint64_t max_spins,
                                                        int32_t* d_status, sar_stream_t stream) {
-    // Without a caller status word the internal one is cleared first, so that
-    // a timeout of an earlier call does not end this call's polls at once.
-    return sar::ll_fixed_scratch_allreduce(in, out, nranks, count, dtype, max_spins, d_status, true,
-                                           reinterpret_cast<cudaStream_t>(stream));
+    return sar::fixed_scratch_allreduce(in, out, nranks, count, dtype, max_spins, d_status,
+                                        reinterpret_cast<cudaStream_t>(stream));
 }

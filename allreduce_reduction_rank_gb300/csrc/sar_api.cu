@@ -38,17 +38,19 @@ bool valid_dtype(int dt) { return dt >= SAR_BF16 && dt <= SAR_FP8_E4M3B15; }
 bool is_fp8(int dt) { return dt == SAR_FP8_E4M3FN || dt == SAR_FP8_E4M3B15; }
 
 // Poll bound of sar_allreduce with SAR_ALGO_LL_ALLPAIR (re-reads of one packet,
-// with sleeps of up to about a microsecond between them).
-constexpr uint64_t kFixedScratchSpins = uint64_t(1) << 20;
+// with sleeps of up to about a microsecond between them).  Every packet a poll
+// waits for is sent by the same CTA, so the bound is never reached.
+constexpr uint64_t kAllpairSpins = uint64_t(1) << 20;
 
-// SAR_ALGO_LL_ALLPAIR takes the one-CTA kernel from 4 ranks up to
-// kCtaAllpairBytes and the cluster kernels up to kClusterAllpairBytes over all
-// ranks (N x S).  Measured against the cluster kernels (fp32, CUDA graph, us
-// per call): 8 x 1 KiB 1.42 / 1.77, 4 x 2 KiB 1.42 / 1.55, 4 x 1 KiB 1.31 /
-// 1.38, 2 x 4 KiB 1.51 / 1.43 (2 ranks stay with the clusters), 16 x 1 KiB
-// and 2 x 8 KiB slower in one CTA (one SM carries all of the call).
+// SAR_ALGO_LL_ALLPAIR runs the sliced shared-memory kernel, except for rank
+// counts without an unrolled kernel (3, 5, 6, 7, 9, ...) from 4 ranks up to
+// kCtaAllpairBytes over all ranks (N x S), which run in one CTA.  Measured
+// (CUDA graph, us per call, one CTA / sliced): 8 x 1 KiB fp32 1.56 / 1.26,
+// 4 x 2 KiB 1.56 / 1.13, 5 x 1 KiB 1.78 / 1.87, 6 x 1 KiB 1.86 / 1.98,
+// 7 x 1 KiB 1.87 / 2.04.
 constexpr size_t kCtaAllpairBytes = size_t(8) << 10;
-constexpr size_t kClusterAllpairBytes = size_t(256) << 10;
+
+bool unrolled_nranks(int n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -215,38 +217,24 @@ SAR_API size_t sar_rsag_chunk(size_t count, int nranks, sar_dtype dtype) {
 SAR_API sar_status sar_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
                                  sar_dtype dtype, sar_algo algo, sar_stream_t stream) {
     if (algo == SAR_ALGO_LL_ALLPAIR) {
-        // Small calls run in one launch without any scratch: every rank's
-        // packets in the shared memory of one CTA for the smallest calls,
-        // else in the shared memory of thread-block clusters up to 256 KiB
-        // over all ranks (the fastest LL forms at those sizes).  Every packet a poll
-        // waits for is sent by the same launch, so no status word is needed.
-        const size_t es = valid_dtype(dtype) ? esize_of(dtype) : 0;
-        const bool small = es != 0 && nranks >= 1 && nranks <= SAR_MAX_RANKS && count_fits(count, es);
-        const bool cta = small && nranks >= 4 && count * es * static_cast<size_t>(nranks) <= kCtaAllpairBytes &&
-                         ll_cta_slot_bytes(nranks, count, dtype) <= kLLCtaMaxSlotBytes;
-        const bool cluster = small && nranks <= SAR_LL_CLUSTER_MAX_RANKS &&
-                             count * es * static_cast<size_t>(nranks) <= kClusterAllpairBytes;
-        if (cta || cluster) {
-            RankPtrs p;
-            bool vec = false, launch = false;
-            const sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
-            if (st != SAR_OK || !launch) return st;
-            bool in16 = true, out16 = true;
-            for (int r = 0; r < nranks; ++r) {
-                in16 = in16 && aligned(in[r], 16);
-                out16 = out16 && aligned(out[r], 16);
-            }
-            cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-            if (cta)
-                return to_status(launch_ll_cta(dtype, nranks, p, count, kFixedScratchSpins, nullptr, in16, out16, s));
-            return to_status(launch_ll_cluster(dtype, nranks, p, count, kFixedScratchSpins, nullptr, in16, out16, s));
+        // One launch, every packet in the shared memory of the CTA that made
+        // and polls it: no scratch and no state, so calls may overlap and be
+        // captured anywhere.
+        RankPtrs p;
+        bool vec = false, launch = false;
+        const sar_status st = check_rsag(in, out, nranks, count, dtype, true, &p, &vec, &launch);
+        if (st != SAR_OK || !launch) return st;
+        bool in16 = true, out16 = true;
+        for (int r = 0; r < nranks; ++r) {
+            in16 = in16 && aligned(in[r], 16);
+            out16 = out16 && aligned(out[r], 16);
         }
-        // Larger calls: two launches on the fixed scratch in stream order, so
-        // no poll ever waits; the bound only ends polls of calls that race on
-        // the shared scratch.  Their timeout goes to the internal status word,
-        // which nothing reads, so it is not cleared per call.
-        return ll_fixed_scratch_allreduce(in, out, nranks, count, dtype, kFixedScratchSpins, nullptr, false,
-                                          reinterpret_cast<cudaStream_t>(stream));
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (!unrolled_nranks(nranks) && nranks >= 4 &&
+            count * esize_of(dtype) <= kCtaAllpairBytes / static_cast<size_t>(nranks) &&
+            ll_cta_slot_bytes(nranks, count, dtype) <= kLLCtaMaxSlotBytes)
+            return to_status(launch_ll_cta(dtype, nranks, p, count, kAllpairSpins, nullptr, in16, out16, s));
+        return to_status(launch_ll_slice(dtype, nranks, p, count, kAllpairSpins, nullptr, in16, out16, s));
     }
     if (algo != SAR_ALGO_RSAG && algo != SAR_ALGO_RSAG_TWO_PHASE) {
         if (!supported_nranks(nranks)) return SAR_ERR_UNSUPPORTED_NRANKS;

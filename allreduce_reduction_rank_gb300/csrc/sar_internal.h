@@ -90,14 +90,6 @@ cudaError_t launch_ll_writeback(sar_dtype dt, int nranks, const RankPtrs& data, 
                                 size_t count, uint32_t epoch, uint64_t* ctrl, bool multi_dest, uint64_t max_spins,
                                 int32_t* status, bool in16, bool out16, cudaStream_t stream);
 
-// The LL allreduce (pack, then unpack-reduce) on the packet scratch compiled
-// into the library (noalloc.cu), with a fresh epoch per call and device.
-// d_status == nullptr: the internal status word, cleared first when
-// clear_internal_status.  Validates its arguments itself.
-sar_status ll_fixed_scratch_allreduce(const void* const* in, void* const* out, int nranks, size_t count,
-                                      sar_dtype dtype, uint64_t max_spins, int32_t* d_status,
-                                      bool clear_internal_status, cudaStream_t stream);
-
 // Test support for the fixed scratch (not exported from the library; a test
 // program links the object files): sets the last epoch used on `dev` and
 // returns the array's device address there (nullptr if it was not looked up).
@@ -115,6 +107,10 @@ constexpr size_t kLLCtaMaxSlotBytes = size_t(64) << 10;
 size_t ll_cta_slot_bytes(int nranks, size_t count, sar_dtype dt);
 cudaError_t launch_ll_cta(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
                           int32_t* status, bool in16, bool out16, cudaStream_t stream);
+// The same over a grid: CTA b plays every rank for one slice of the packets
+// (ll_cta.cu); any size, no scratch.
+cudaError_t launch_ll_slice(sar_dtype dt, int nranks, const RankPtrs& p, size_t count, uint64_t max_spins,
+                            int32_t* status, bool in16, bool out16, cudaStream_t stream);
 
 cudaError_t launch_convert(const void* src, sar_dtype src_dt, void* dst, sar_dtype dst_dt,
                            size_t count, bool vec, cudaStream_t stream);

@@ -232,6 +232,9 @@ def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, gr
     if g is not None:
         row["graph_us"] = round(g * 1e3, 3)
         row["graph_GBps"] = round(wl.algo_bytes / (g * 1e-3) / GB, 1)
+    if algo == 2:      # the LL rows' check: the outputs equal the rsag allreduce
+        want = rsag_result(torch, sar, din, wl, stream)
+        row["outputs_ok"] = all(torch.equal(o.view(torch.uint8), want.view(torch.uint8)) for o in dout)
     del din, dout
     return row
 

@@ -26,10 +26,9 @@
  *    copies the pointers into kernel parameters, keeps no caller pointer after
  *    the call returns, allocates nothing and does not synchronise (except
  *    sar_read_device_status), so calls are stream-ordered and may be captured
- *    into a CUDA graph.  The only state kept between calls belongs to the LL
- *    path on the library's fixed packet scratch (SAR_ALGO_LL_ALLPAIR and
- *    sar_allreduce_ll_noalloc): the scratch array itself and, per device, its
- *    address and last epoch.
+ *    into a CUDA graph.  The only state kept between calls belongs to
+ *    sar_allreduce_ll_noalloc: the fixed packet scratch compiled into the
+ *    library and, per device, its address and last epoch.
  *  - `count` is the number of elements per rank.  count == 0 returns SAR_OK
  *    without launching anything.
  *  - Every argument error is returned before any launch.  nranks may be any
@@ -92,7 +91,7 @@ typedef enum {
 typedef enum {
     SAR_ALGO_RSAG = 0,            /* one fused kernel: reduce chunk, write to all outputs */
     SAR_ALGO_RSAG_TWO_PHASE = 1,  /* reduce-scatter kernel, then all-gather kernel */
-    SAR_ALGO_LL_ALLPAIR = 2       /* LL all-pair packets on the library's fixed scratch */
+    SAR_ALGO_LL_ALLPAIR = 2       /* LL all-pair packets in shared memory, one launch */
 } sar_algo;
 
 typedef enum {
@@ -124,26 +123,20 @@ typedef enum {
  * then sar_all_gather.
  *
  * SAR_ALGO_LL_ALLPAIR runs the LL all-pair allreduce (mscclpp commit history,
- * the allreduce_allpair_packet fix), in the fastest of three forms for the
- * size (all give the same bits):
- *  - nranks >= 4 and nranks * S <= 8 KiB: one CTA plays every rank, the
- *    packets in its shared memory (no scratch, no state);
- *  - otherwise, nranks <= SAR_LL_CLUSTER_MAX_RANKS and nranks * S <= 256 KiB:
- *    the cluster form of sar_allreduce_ll_cluster (packets through shared
- *    memory, no scratch, no state);
- *    calls of these two forms may also overlap on the GPU;
- *  - otherwise sar_ll_pack then sar_ll_unpack_reduce, stream-ordered, on the
- *    packet scratch compiled into the library (the array that
- *    sar_allreduce_ll_noalloc uses, with a fresh epoch per call).  That form
- *    takes only the sizes that fit the array (nranks *
- *    sar_ll_packet_bytes(count, dtype) rounded up to 256 bytes per rank at
- *    most SAR_LL_NOALLOC_SCRATCH_BYTES, e.g. up to 1 MiB per rank with 8
- *    ranks); larger calls return SAR_ERR_INVALID_ARG before any launch.  The
- *    first such call on a device looks up the array's address; make it before
- *    any CUDA graph capture on that device.  In stream order every packet a
- *    call polls was written by the same call's pack kernel, so the polls never
- *    wait.  Calls that overlap on the GPU (two streams without ordering) share
- *    the array and race: their outputs are undefined.
+ * the allreduce_allpair_packet fix: send, reduce and write-back in the same
+ * thread block, packets checked by their flags) in one launch, with every
+ * packet in the shared memory of the CTA that makes and polls it:
+ *  - by default, CTA b plays every rank for one slice of the packets: it turns
+ *    the slice of each rank's input into {payload, flag} packets in its
+ *    shared memory, polls each packet's flag, reduces in rank order and writes
+ *    the result to all N outputs, so a call of any size spreads over the SMs;
+ *  - for rank counts without an unrolled kernel (3, 5, 6, 7, 9, ...) from 4
+ *    ranks up to 8 KiB over all ranks (nranks * S), one CTA plays every rank
+ *    for the whole call (measured faster there).
+ * Neither form uses scratch or keeps state: calls may overlap on the GPU and
+ * may be captured into a CUDA graph at any time.  Every packet a poll waits
+ * for is sent by the same CTA, so the polls' bound is never reached in a
+ * correct call.  Any size whose buffers exist is accepted.
  *
  * All three algorithms give the same bits.
  *

@@ -210,10 +210,10 @@ int main(void) {
     EXPECT(sar_allreduce(in, out, 2, 0, SAR_BF16, SAR_ALGO_RSAG, NULL), SAR_OK);
     EXPECT(sar_allreduce(in, out, 33, 16, SAR_FP32, SAR_ALGO_LL_ALLPAIR, NULL), SAR_ERR_UNSUPPORTED_NRANKS);
     EXPECT(sar_allreduce(in, out, 2, 0, SAR_FP32, SAR_ALGO_LL_ALLPAIR, NULL), SAR_OK);
-    /* 2^20 + 1 fp32 elements per rank need 8 MiB + 8 bytes of packets: two ranks overflow the
-       16 MiB fixed scratch */
-    EXPECT(sar_allreduce(in, out, 2, ((size_t)1 << 20) + 1, SAR_FP32, SAR_ALGO_LL_ALLPAIR, NULL),
-           SAR_ERR_INVALID_ARG);
+    {
+        const void* odd[2] = {(const void*)(uintptr_t)4098, (const void*)(uintptr_t)8192};
+        EXPECT(sar_allreduce(odd, out, 2, 16, SAR_FP32, SAR_ALGO_LL_ALLPAIR, NULL), SAR_ERR_MISALIGNED);
+    }
     EXPECT(sar_allreduce(in, out, 2, 16, SAR_FP32, (sar_algo)3, NULL), SAR_ERR_INVALID_ARG);
     EXPECT(sar_ll_pack(in, out, 2, 16, SAR_BF16, 0, NULL), SAR_ERR_INVALID_ARG);
     EXPECT(sar_read_device_status(NULL, NULL), SAR_ERR_INVALID_ARG);

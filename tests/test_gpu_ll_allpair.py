@@ -1,9 +1,10 @@
 """GPU parity of sar_allreduce with SAR_ALGO_LL_ALLPAIR: the LL all-pair
-packet allreduce behind the one allreduce entry point, in one CTA's shared
-memory for the smallest calls, through cluster shared memory for small ones
-and on the library's fixed packet scratch for larger ones.  Bar: bit-exact
-against the oracle (NaN by class), canaries intact, inputs unchanged; sizes
-beyond the fixed scratch are refused before any launch."""
+packet allreduce behind the one allreduce entry point, every packet in the
+shared memory of the CTA that makes and polls it (one slice of the packets
+per CTA, or one CTA for the whole call for small calls of rank counts without
+an unrolled kernel).  Bar: bit-exact against the oracle (NaN by class),
+canaries intact, inputs unchanged, at any size and with calls overlapping on
+two streams."""
 import numpy as np
 import pytest
 import torch
@@ -57,9 +58,10 @@ def test_ll_allpair_matches_oracle(sar, dt, n, count):
 
 @pytest.mark.parametrize("n", [4, 5, 8, 16, 31])
 @pytest.mark.parametrize("dt", DTYPES)
-def test_ll_allpair_one_cta_sizes(sar, dt, n):
-    """Calls of at most 8 KiB over all ranks, from 4 ranks up, run in one
-    CTA: ragged counts up to that size, aligned and at odd element offsets."""
+def test_ll_allpair_small_sizes(sar, dt, n):
+    """Calls of at most 8 KiB over all ranks (one CTA for 5 and 31 ranks, one
+    or a few slices otherwise): ragged counts up to that size, aligned and at
+    odd element offsets."""
     limit = (8 << 10) // n // ESIZE[dt]
     rng = np.random.default_rng([DTYPES.index(dt), n, 31])
     for count in (1, 5, limit // 2 + 1, limit):
@@ -94,7 +96,7 @@ def test_ll_allpair_in_place(sar):
 def test_ll_allpair_config5_sizes_back_to_back(sar):
     """8 ranks, fp32 and bf16, 1 KiB to 1 MiB per rank (the LL workloads),
     called back to back without synchronising: each call's outputs equal the
-    oracle's, although every call reuses the same fixed scratch."""
+    oracle's."""
     outs = []
     for w in W.C5:
         ins = w.inputs()
@@ -109,9 +111,8 @@ def test_ll_allpair_config5_sizes_back_to_back(sar):
 
 
 def test_ll_allpair_in_a_cuda_graph(sar):
-    """Captured once (after an eager call has set the scratch up on this
-    device) and replayed on new inputs: the replays re-pack before they
-    poll, so each gives the sum of the inputs it saw."""
+    """Captured once and replayed on new inputs: each replay makes its packets
+    afresh before it polls them, so each gives the sum of the inputs it saw."""
     n, count, dt = 8, 5000, "fp32"
     rng = np.random.default_rng(9)
     gin = [Guarded(count * 4) for _ in range(n)]
@@ -136,28 +137,68 @@ def test_ll_allpair_in_a_cuda_graph(sar):
             assert_same(g.codes(dt), want, dt)
 
 
-@pytest.mark.parametrize("total", [8 << 10, 256 << 10], ids=["cta_to_cluster", "cluster_to_scratch"])
-@pytest.mark.parametrize("n,dt", [(8, "fp32"), (16, "bf16"), (2, "e4m3fn"), (32, "fp16")])
-def test_ll_allpair_forms_at_the_size_thresholds(sar, n, dt, total):
-    """Up to 8 KiB over all ranks (from 4 ranks) the call runs in one CTA, up
-    to 256 KiB in clusters (at most 16 ranks), above that as two launches on
-    the fixed scratch: exact on either side of each threshold."""
-    per_rank = total // n // ESIZE[dt]
-    for count in (per_rank, per_rank + 1):
-        rng = np.random.default_rng([n, count])
-        ins = [random_codes(rng, dt, count) for _ in range(n)]
-        want = oracle.allreduce(ins, dt)[0]
-        gin, gout = _run(sar, ins, dt)
-        _check(gin, gout, ins, want, dt)
+@pytest.mark.parametrize("n,dt,count", [
+    (5, "fp32", (8 << 10) // 5 // 4), (5, "fp32", (8 << 10) // 5 // 4 + 1),      # one CTA -> slices
+    (31, "e4m3fn", (8 << 10) // 31), (31, "e4m3fn", (8 << 10) // 31 + 1),
+    (8, "fp32", 151 * 512), (8, "fp32", 151 * 512 + 1),                           # 1 -> 4 packets per thread
+    (2, "bf16", 2 * 151 * 512), (2, "bf16", 2 * 151 * 512 + 2),
+    (16, "fp16", 2 * 151 * 512 + 2)])                                             # 16 ranks: 1 packet per thread
+def test_ll_allpair_forms_at_their_boundaries(sar, n, dt, count):
+    """Exact on either side of each switch between forms: one CTA for the
+    whole call (rank counts without an unrolled kernel, at most 8 KiB over
+    all ranks), slices of 1 packet per thread, slices of 4 packets per thread
+    (at most 8 ranks, from 152 slices of 512 packets per rank)."""
+    rng = np.random.default_rng([n, count])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt)
+    _check(gin, gout, ins, want, dt)
 
 
-def test_ll_allpair_rejects_sizes_beyond_the_scratch(sar):
+def test_ll_allpair_large_call(sar):
+    """8 ranks x 8 MiB + 20 bytes of fp32 (64 MiB of packets, more than the
+    fixed scratch of the no-alloc entry point holds): accepted and exact."""
+    n, dt, count = 8, "fp32", (2 << 20) + 5
+    rng = np.random.default_rng(4242)
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout = _run(sar, ins, dt)
+    _check(gin, gout, ins, want, dt)
+
+
+def test_ll_allpair_calls_on_two_streams_overlap_safely(sar):
+    """No scratch and no state: calls on two streams without any ordering
+    between them may run at the same time, and both give the oracle's
+    outputs (sizes of one slice, several slices of 1 packet per thread and
+    slices of 4 packets per thread)."""
+    n, dt = 8, "fp32"
+    rng = np.random.default_rng(23)
+    for count in (256, 16384, 262144):
+        cases = []
+        for _ in range(2):
+            ins = [random_codes(rng, dt, count) for _ in range(n)]
+            gin = [Guarded.from_codes(c) for c in ins]
+            gout = [Guarded(count * 4) for _ in range(n)]
+            cases.append((ins, gin, gout, torch.cuda.Stream()))
+        torch.cuda.synchronize()
+        for _ in range(30):
+            for ins, gin, gout, stream in cases:
+                sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout], count=count, dtype=dt, algo=LL,
+                                  stream=stream)
+        torch.cuda.synchronize()
+        for ins, gin, gout, stream in cases:
+            _check(gin, gout, ins, oracle.allreduce(ins, dt)[0], dt)
+
+
+def test_ll_allpair_argument_errors(sar):
     L = sar.lib
     n, dt = 8, "fp32"
     bufs = [Guarded(64) for _ in range(n)]
-    fits = sar.SAR_LL_NOALLOC_SCRATCH_BYTES // n // 8 * 4 // ESIZE[dt]
     import ctypes
     arr = (ctypes.c_void_p * n)(*[b.ptr for b in bufs])
-    assert L.sar_allreduce(arr, arr, n, fits + 1, sar.DTYPE_CODES[dt], LL, None) == sar.SAR_ERR_INVALID_ARG
+    odd = (ctypes.c_void_p * n)(*([bufs[0].ptr + 2] + [b.ptr for b in bufs[1:]]))
     assert L.sar_allreduce(arr, arr, 33, 16, sar.DTYPE_CODES[dt], LL, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce(arr, arr, 0, 16, sar.DTYPE_CODES[dt], LL, None) == sar.SAR_ERR_UNSUPPORTED_NRANKS
+    assert L.sar_allreduce(odd, arr, n, 16, sar.DTYPE_CODES[dt], LL, None) == sar.SAR_ERR_MISALIGNED
+    assert L.sar_allreduce(arr, arr, n, 16, 7, LL, None) == sar.SAR_ERR_UNSUPPORTED_DTYPE
     assert L.sar_allreduce(arr, arr, n, 0, sar.DTYPE_CODES[dt], LL, None) == sar.SAR_OK

@@ -164,8 +164,8 @@ def test_cluster_argument_errors(sar):
 def test_cluster_calls_on_two_streams_overlap_safely(sar):
     """The cluster form keeps no state between calls, so calls on two streams
     without any ordering between them may run at the same time; both give
-    the oracle's outputs (sar_allreduce_ll_cluster directly, and
-    SAR_ALGO_LL_ALLPAIR at a size that takes the cluster form)."""
+    the oracle's outputs (interleaved with SAR_ALGO_LL_ALLPAIR calls on the
+    same streams, which keep no state either)."""
     n, count, dt = 8, 4096, "fp32"
     rng = np.random.default_rng(17)
     cases = []
