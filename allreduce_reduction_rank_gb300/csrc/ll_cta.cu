@@ -199,11 +199,19 @@ cudaError_t cta_ranks(int nranks, const RankPtrs& p, size_t count, uint64_t max_
 //            0..N-1 in binary32, rounds once and writes the result (16 bytes
 //            for PPT = 4, 4 for PPT = 1) to all N outputs.
 // ---------------------------------------------------------------------------
+// Slot of packet q (0..SP-1) of a slice in its rank's row: packets 0-1 of
+// every group of 4 in the first half of the row, packets 2-3 in the second,
+// so that the 16-byte accesses of a warp (two packets of consecutive groups)
+// are contiguous and free of bank conflicts.
+template <int SP> __device__ __forceinline__ int slice_slot(int q) {
+    return ((q & 3) >> 1) * (SP / 2) + (q >> 2) * 2 + (q & 1);
+}
+
 template <int DT, int NR, int CT, int PPT>
 __global__ void __launch_bounds__(CT)
 slice_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t max_spins, int32_t* status, bool in16,
              bool out16) {
-    extern __shared__ __align__(16) uint64_t slots[];   // [rank k][SP]
+    extern __shared__ __align__(16) uint64_t slots[];   // [rank k][slice_slot(q)]
     constexpr int SP = PPT * CT;
     constexpr int G = SP / 4;                           // input vectors per rank in a slice
     constexpr int EP = PerWord<DT>::kN;
@@ -239,12 +247,12 @@ slice_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t m
             const int it = threadIdx.x + (u0 + u) * CT;
             const int k = it / G, g = (it + 32 * k) % G;
             if (it >= items || 4 * g >= np) continue;
-            uint64_t* row = slots + k * SP + 4 * g;
+            uint64_t* row = slots + k * SP;
             if (4 * g + 4 <= np) {
-                st_slot4(row, packet(x[u][0]), packet(x[u][1]));
-                st_slot4(row + 2, packet(x[u][2]), packet(x[u][3]));
+                st_slot4(row + slice_slot<SP>(4 * g), packet(x[u][0]), packet(x[u][1]));
+                st_slot4(row + slice_slot<SP>(4 * g + 2), packet(x[u][2]), packet(x[u][3]));
             } else {
-                for (int m = 0; m < 4 && 4 * g + m < np; ++m) st_slot(row + m, packet(x[u][m]));
+                for (int m = 0; m < 4 && 4 * g + m < np; ++m) st_slot(row + slice_slot<SP>(4 * g + m), packet(x[u][m]));
             }
         }
     }
@@ -260,13 +268,13 @@ slice_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t m
 #pragma unroll
         for (int k = 0; k < WIN; ++k) {
             if (NR == 0 && k0 + k >= n) break;
-            const uint64_t* row = slots + (k0 + k) * SP + t0;
+            const uint64_t* row = slots + (k0 + k) * SP;
             if (PPT == 4 && mn >= 4) {
-                ld_slot2(row, pk[k][0], pk[k][PPT > 1 ? 1 : 0]);
-                ld_slot2(row + 2, pk[k][PPT > 2 ? 2 : 0], pk[k][PPT > 3 ? 3 : 0]);
+                ld_slot2(row + slice_slot<SP>(t0), pk[k][0], pk[k][PPT > 1 ? 1 : 0]);
+                ld_slot2(row + slice_slot<SP>(t0 + 2), pk[k][PPT > 2 ? 2 : 0], pk[k][PPT > 3 ? 3 : 0]);
             } else {
 #pragma unroll
-                for (int m = 0; m < PPT; ++m) pk[k][m] = m < mn ? ld_slot(row + m) : packet(0);
+                for (int m = 0; m < PPT; ++m) pk[k][m] = m < mn ? ld_slot(row + slice_slot<SP>(t0 + m)) : packet(0);
             }
         }
         unsigned ns = 32;
@@ -294,7 +302,7 @@ slice_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t m
 #pragma unroll
                 for (int m = 0; m < PPT; ++m)
                     if (static_cast<uint32_t>(pk[k][m] >> 32) != kFlag)
-                        pk[k][m] = ld_slot(slots + (k0 + k) * SP + t0 + m);
+                        pk[k][m] = ld_slot(slots + (k0 + k) * SP + slice_slot<SP>(t0 + m));
             }
         }
         if (!ok) break;
