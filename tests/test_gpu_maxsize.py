@@ -102,3 +102,26 @@ def test_cluster_ll_past_2_32_elements(sar):
         assert torch.equal(dout[j], dout[0])
     del din, dout
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n,count", [(2, (1 << 32) + 4099), (16, (1 << 31) + 4099)],
+                         ids=["2_ranks_4_packets_per_thread", "16_ranks_1_packet_per_thread"])
+def test_ll_allpair_past_2_31_bytes(sar, n, count):
+    """sar_allreduce with SAR_ALGO_LL_ALLPAIR (e4m3fn) past 2^32 elements per
+    rank with 2 ranks (slices of 4 packets per thread, slice offsets past
+    2^30 packets) and past 2^31 bytes per rank with 16 ranks (slices of 1
+    packet per thread)."""
+    dt = "e4m3fn"
+    pats = W.rank_inputs("normal", 10 + n, dt, P, n, 4.0)
+    din = [_tiled(p, count, torch.uint8) for p in pats]
+    dout = [torch.empty_like(din[0]) for _ in range(n)]
+    sar.sar_allreduce(din, dout, count=count, dtype=dt, algo=sar.SAR_ALGO_LL_ALLPAIR)
+    torch.cuda.synchronize()
+    idx = _indices(count, n, dt, np.random.default_rng(n))
+    want = oracle.allreduce([p[idx % P] for p in pats], dt)[0]
+    tidx = torch.from_numpy(idx).cuda()
+    for j in range(n):
+        assert np.array_equal(dout[j][tidx].cpu().numpy(), want)
+        assert torch.equal(dout[j], dout[0])
+    del din, dout
+    torch.cuda.empty_cache()
