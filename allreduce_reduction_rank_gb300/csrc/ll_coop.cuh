@@ -1,6 +1,8 @@
-// ll_coop.cuh -- the LL all-pair allreduce as one cooperative launch: the
-// kernel template shared by sar_allreduce_ll_fused (ll_fused.cu) and
-// sar_allreduce_ll_writeback (ll_writeback.cu).
+// ll_coop.cuh -- the LL all-pair allreduce in one launch: the kernels shared
+// by sar_allreduce_ll_fused (ll_fused.cu) and sar_allreduce_ll_writeback
+// (ll_writeback.cu).  Calls up to a size limit (direct and multi-destination
+// write-backs) run the sliced form further down, in which every block plays
+// all ranks for one slice of the packets; the others run the cooperative form:
 //
 // mscclpp commit history, the allreduce_allpair_packet fix: the same thread
 // block sends, reduces and writes back.  Every block of simulated rank r
@@ -24,8 +26,9 @@
 //      whole groups of 4 packets, so a group never spans two chunks.
 // Each 8-byte packet is one single-copy-atomic store and load, so a flag that
 // matches the epoch guarantees its payload; a stale flag means "not arrived".
-// Every poll is bounded.  Blocks wait on one another, so the launch is
-// cooperative: the runtime makes every block co-resident or refuses the launch.
+// Every poll is bounded.  In this form blocks wait on one another, so the
+// launch is cooperative: the runtime makes every block co-resident or refuses
+// the launch.
 //
 // Epochs: the caller's, or a device counter (commit history, the flag buffer
 // change: one flag buffer shared by the algorithms) that every launch advances
@@ -337,6 +340,314 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
 
 }
 
+// ---------------------------------------------------------------------------
+// Sliced form (kDirect and kPacketsAll): block b plays every rank for packets
+// [b*SP, (b+1)*SP) of the buffers (SP = PPT*kSliceThreads packets per rank),
+// so no block waits for another and the launch needs no co-residency.  In a
+// slice:
+//   A. item (k, g) packs input vector g of the slice of rank k into pkts[k]
+//      (items spread over the threads, rotated by a warp per rank, so the
+//      packets a warp polls come from other warps; the loads of up to 8
+//      items are issued before their packet stores);
+//   B. thread t polls packets PPT*t .. PPT*t+PPT-1 of every rank (windows of
+//      up to 8 ranks polled together), adds in rank order, rounds once;
+//   C. kDirect: plain stores of the result to all N outputs; kPacketsAll: the
+//      result as flagged packets into `res`, then thread t polls the result
+//      packets another warp wrote and writes each, read once, to all N
+//      outputs.
+// The packet and result-packet images are those of the cooperative form.
+// Measured against it (8 ranks fp32, CUDA graph, us per call, cooperative /
+// sliced): direct write-back 1 KiB 2.30 / 1.90, 64 KiB 2.89 / 2.18, 256 KiB
+// 3.72 / 3.04, 1 MiB 6.44 / 6.74; multi-destination packet write-back 1 KiB
+// 2.73 / 2.14, 256 KiB 4.56 / 3.48, 1 MiB 8.28 / 7.59, 4 MiB 26.6 / 44.2;
+// per-output packet write-back (result packets read once per output rank)
+// 1 KiB 2.72 / 2.91, 256 KiB 4.49 / 5.83, so that one stays cooperative.  4
+// packets per thread (16-byte stores, 128 registers) was slower at 1 MiB
+// (7.38 us direct).
+// ---------------------------------------------------------------------------
+constexpr int kSliceThreads = 128;
+constexpr int kSlicePackets = 1;          // packets per thread and rank
+// Largest bytes per rank that run sliced.
+constexpr size_t kSliceDirectMaxBytes = size_t(256) << 10;
+constexpr size_t kSliceMultiDestMaxBytes = size_t(1) << 20;
+
+template <int N>
+__device__ __forceinline__ bool poll_slot(const uint64_t* src, int m_live, uint32_t epoch, uint64_t max_spins,
+                                          int32_t* status, uint64_t (&w)[N]) {
+    unsigned ns = 32;
+    for (uint64_t spin = 0;; ++spin) {
+        bool ready = true;
+#pragma unroll
+        for (int m = 0; m < N; ++m) ready = ready && (m >= m_live || packet_flag(w[m]) == epoch);
+        if (ready) return true;
+        if (spin >= max_spins) {
+            atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+            return false;
+        }
+        if (spin >= kSpinPolls) {
+            if (ld_status_word(status) != 0) return false;
+            __nanosleep(ns);
+            if (ns < kMaxSleepNs) ns *= 2;
+        }
+#pragma unroll
+        for (int m = 0; m < N; ++m)
+            if (m < m_live && packet_flag(w[m]) != epoch) w[m] = ld_packet(src + m);
+    }
+}
+
+// Result packets [w, w + m_live) of one thread (m_live <= PPT): load them,
+// then (finish_slot) poll until they carry the epoch and store their payloads
+// to outputs [j0, j1).
+template <int PPT>
+__device__ __forceinline__ void load_slot(const uint64_t* res, size_t w, int m_live, uint64_t (&r)[PPT]) {
+    if (PPT == 4 && m_live >= 4) {
+        ld_packets2(res + w, r[0], r[PPT > 1 ? 1 : 0]);
+        ld_packets2(res + w + 2, r[PPT > 2 ? 2 : 0], r[PPT > 3 ? 3 : 0]);
+    } else {
+#pragma unroll
+        for (int m = 0; m < PPT; ++m) r[m] = m < m_live ? ld_packet(res + w + m) : 0;
+    }
+}
+
+template <int DT, int PPT>
+__device__ __forceinline__ bool finish_slot(const LLArgs& a, size_t count, size_t nbytes, size_t w, int m_live, int j0,
+                                            int j1, uint32_t epoch, uint64_t max_spins, int32_t* status, bool out16,
+                                            uint64_t (&r)[PPT]) {
+    constexpr int EP = PerWord<DT>::kN;
+    if (!poll_slot<PPT>(a.res + w, m_live, epoch, max_spins, status, r)) return false;
+    if (out16 && m_live >= PPT && 4 * (w + PPT) <= nbytes) {
+        if constexpr (PPT == 4) {
+            const uint4 y = make_uint4(packet_payload(r[0]), packet_payload(r[1]), packet_payload(r[2]),
+                                       packet_payload(r[3]));
+            for (int j = j0; j < j1; ++j) st_stream(static_cast<uint4*>(a.data.out[j]) + w / 4, y);
+        } else {
+#pragma unroll
+            for (int m = 0; m < PPT; ++m)
+                for (int j = j0; j < j1; ++j)
+                    st_stream_word(static_cast<uint32_t*>(a.data.out[j]) + w + m, packet_payload(r[m]));
+        }
+    } else {
+        for (int m = 0; m < PPT && m < m_live; ++m)
+            for (int j = j0; j < j1; ++j)
+#pragma unroll
+                for (int e = 0; e < EP; ++e)
+                    if ((w + m) * EP + e < count) store_bits<DT>(a.data.out[j], (w + m) * EP + e, packet_payload(r[m]), e);
+    }
+    return true;
+}
+
+// Phase A of the sliced form, in windows of up to 8 items per thread: item
+// it = threadIdx.x + (u0 + u) * CT is input vector g of rank k of the slice
+// starting at packet w0 (np packets).  slice_load issues the loads of a
+// window, slice_store writes their packets.
+template <int G, int CT>
+__device__ __forceinline__ void slice_load(const LLArgs& a, int n, size_t nbytes, bool in16, size_t w0, int np, int u0,
+                                           uint32_t (&x)[8][4]) {
+    const int items = n * G;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int it = threadIdx.x + (u0 + u) * CT;
+        const int k = it / G, g = (it + 32 * k) % G;
+        if (it >= items || 4 * g >= np) continue;
+        const size_t w = w0 + 4 * static_cast<size_t>(g);
+        const unsigned char* src = static_cast<const unsigned char*>(a.data.in[k]);
+        if (in16 && 4 * (w + 4) <= nbytes) {
+            const uint4 q = ld_stream(reinterpret_cast<const uint4*>(src) + w / 4);
+            x[u][0] = q.x; x[u][1] = q.y; x[u][2] = q.z; x[u][3] = q.w;
+        } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) x[u][m] = 4 * g + m < np ? payload_word(src, nbytes, w + m) : 0;
+        }
+    }
+}
+
+template <int G, int CT>
+__device__ __forceinline__ void slice_store(const LLArgs& a, int n, size_t w0, int np, int u0, uint32_t epoch,
+                                            bool pk32, const uint32_t (&x)[8][4]) {
+    const int items = n * G;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int it = threadIdx.x + (u0 + u) * CT;
+        const int k = it / G, g = (it + 32 * k) % G;
+        if (it >= items || 4 * g >= np) continue;
+        uint64_t* dst = a.pkts[k] + w0 + 4 * g;
+        if (4 * g + 4 <= np) {
+            const uint64_t p0 = make_packet(x[u][0], epoch), p1 = make_packet(x[u][1], epoch);
+            const uint64_t p2 = make_packet(x[u][2], epoch), p3 = make_packet(x[u][3], epoch);
+            if (pk32) {
+                st_packets4(dst, p0, p1, p2, p3);
+            } else {
+                st_packets2(dst, p0, p1);
+                st_packets2(dst + 2, p2, p3);
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (4 * g + m < np) st_packet(dst + m, make_packet(x[u][m], epoch));
+        }
+    }
+}
+
+template <int DT, int NR, int WB, int PPT>
+__global__ void __launch_bounds__(kSliceThreads)
+slice_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t slices, uint32_t host_epoch,
+             uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
+    static_assert(WB == kDirect || WB == kPacketsAll, "the per-output write-back is cooperative only");
+    constexpr int CT = kSliceThreads;
+    constexpr int SP = PPT * CT;
+    constexpr int G = SP / 4;
+    constexpr int EP = PerWord<DT>::kN;
+    constexpr int WIN = NR > 0 ? (NR < 8 ? NR : 8) : 8;
+    pdl_wait();
+    const int n = ranks<NR>(n_rt);
+    const size_t npk = (nbytes + 3) / 4;
+    // The first window of input loads is issued before the epoch is known,
+    // so those loads and the epoch counter's atomic are in flight together.
+    uint32_t x[8][4];
+    {
+        const size_t w0 = static_cast<size_t>(blockIdx.x) * SP;
+        slice_load<G, CT>(a, n, nbytes, in16, w0, static_cast<int>(min(static_cast<size_t>(SP), npk - w0)), 0, x);
+    }
+    __shared__ uint32_t s_epoch;
+    if (threadIdx.x == 0) s_epoch = ctrl != nullptr ? take_ticket(ctrl) : host_epoch;
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
+    for (size_t b = blockIdx.x; b < slices; b += gridDim.x) {
+        const size_t w0 = b * SP;
+        const int np = static_cast<int>(min(static_cast<size_t>(SP), npk - w0));
+
+        // A. send
+        for (int u0 = 0; u0 * CT < n * G; u0 += 8) {
+            if (b != blockIdx.x || u0 != 0) slice_load<G, CT>(a, n, nbytes, in16, w0, np, u0, x);
+            slice_store<G, CT>(a, n, w0, np, u0, epoch, pk32, x);
+        }
+
+        // B. poll and reduce
+        const int t0 = PPT * threadIdx.x;
+        const int mn = min(PPT, np - t0);
+        const size_t w = w0 + t0;
+        float acc[PPT][EP];
+        if (mn > 0) {
+#pragma unroll 1
+            for (int k0 = 0; k0 < n; k0 += WIN) {
+                uint64_t pk[WIN][PPT];
+#pragma unroll
+                for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
+                    const uint64_t* row = a.pkts[k0 + k] + w;
+                    if (PPT == 4 && mn >= 4) {
+                        ld_packets2(row, pk[k][0], pk[k][PPT > 1 ? 1 : 0]);
+                        ld_packets2(row + 2, pk[k][PPT > 2 ? 2 : 0], pk[k][PPT > 3 ? 3 : 0]);
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < PPT; ++m) pk[k][m] = m < mn ? ld_packet(row + m) : 0;
+                    }
+                }
+                unsigned ns = 32;
+                for (uint64_t spin = 0;; ++spin) {
+                    bool ready = true;
+#pragma unroll
+                    for (int k = 0; k < WIN; ++k) {
+                        if (NR == 0 && k0 + k >= n) break;
+#pragma unroll
+                        for (int m = 0; m < PPT; ++m) ready = ready && (m >= mn || packet_flag(pk[k][m]) == epoch);
+                    }
+                    if (ready) break;
+                    if (spin >= max_spins) {
+                        atomicCAS(status, 0, static_cast<int32_t>(SAR_ERR_TIMEOUT));
+                        return;
+                    }
+                    if (spin >= kSpinPolls) {
+                        if (ld_status_word(status) != 0) return;
+                        __nanosleep(ns);
+                        if (ns < kMaxSleepNs) ns *= 2;
+                    }
+#pragma unroll
+                    for (int k = 0; k < WIN; ++k) {
+                        if (NR == 0 && k0 + k >= n) break;
+#pragma unroll
+                        for (int m = 0; m < PPT; ++m)
+                            if (m < mn && packet_flag(pk[k][m]) != epoch) pk[k][m] = ld_packet(a.pkts[k0 + k] + w + m);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < WIN; ++k) {
+                    if (NR == 0 && k0 + k >= n) break;
+#pragma unroll
+                    for (int m = 0; m < PPT; ++m) {
+                        float xv[EP];
+                        widen_word<DT>(packet_payload(pk[k][m]), xv);
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) acc[m][e] = (k0 + k == 0) ? xv[e] : __fadd_rn(acc[m][e], xv[e]);
+                    }
+                }
+            }
+
+            // C. write-back
+            if constexpr (WB == kDirect) {
+                if (out16 && mn >= PPT && 4 * (w + PPT) <= nbytes) {
+                    if constexpr (PPT == 4) {
+                        const uint4 y = make_uint4(narrow_word<DT>(acc[0]), narrow_word<DT>(acc[PPT > 1 ? 1 : 0]),
+                                                   narrow_word<DT>(acc[PPT > 2 ? 2 : 0]),
+                                                   narrow_word<DT>(acc[PPT > 3 ? 3 : 0]));
+                        for (int j = 0; j < n; ++j) st_stream(static_cast<uint4*>(a.data.out[j]) + w / 4, y);
+                    } else {
+                        const uint32_t y = narrow_word<DT>(acc[0]);
+                        for (int j = 0; j < n; ++j) st_stream_word(static_cast<uint32_t*>(a.data.out[j]) + w, y);
+                    }
+                } else {
+                    for (int m = 0; m < PPT && m < mn; ++m)
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) {
+                            const size_t i = (w + m) * EP + e;
+                            if (i < count)
+                                for (int j = 0; j < n; ++j) store_elem<DT>(a.data.out[j], i, acc[m][e]);
+                        }
+                }
+            } else {
+                // Elements past the end are zero bits, as in the send's padding.
+                for (int m = 0; m < PPT && m < mn; ++m) {
+                    float xs[EP];
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) xs[e] = ((w + m) * EP + e < count) ? acc[m][e] : 0.0f;
+                    st_packet(a.res + w + m, make_packet(narrow_word<DT>(xs), epoch));
+                }
+            }
+        }
+        if constexpr (WB == kPacketsAll) {
+            // Result packets of the thread one warp further on: each read once
+            // and written to every output.
+            const int tr = (threadIdx.x + 32) % CT;
+            const int mr = min(PPT, np - PPT * tr);
+            if (mr > 0) {
+                uint64_t r[PPT];
+                load_slot<PPT>(a.res, w0 + PPT * tr, mr, r);
+                if (!finish_slot<DT, PPT>(a, count, nbytes, w0 + PPT * tr, mr, 0, n, epoch, max_spins, status, out16,
+                                          r))
+                    return;
+            }
+        }
+    }
+}
+
+// Blocks of the sliced form: one per slice, at most kMaxSliceBlocks (then each
+// block takes several slices in turn; a launch's tickets stay below 2^20).
+constexpr size_t kMaxSliceBlocks = size_t(1) << 16;
+
+template <int DT, int NR, int WB>
+cudaError_t slice_launch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
+                         uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
+    constexpr int PPT = kSlicePackets;
+    const size_t nbytes = count * Elem<DT>::kSize;
+    const size_t npk = (nbytes + 3) / 4;
+    const size_t slices = (npk + PPT * kSliceThreads - 1) / (PPT * kSliceThreads);
+    const unsigned blocks = static_cast<unsigned>(std::min(slices, kMaxSliceBlocks));
+    bool p32 = true;
+    for (int r = 0; r < nranks; ++r) p32 = p32 && reinterpret_cast<uintptr_t>(a.pkts[r]) % 32 == 0;
+    return launch_kernel(slice_kernel<DT, NR, WB, PPT>, dim3(blocks), dim3(kSliceThreads), s, a, nranks, count,
+                         nbytes, slices, epoch, ctrl, max_spins, status, in16, out16, p32);
+}
+
 inline unsigned div_up(size_t a, size_t b) { return static_cast<unsigned>((a + b - 1) / b); }
 
 template <int DT, int NR, int WB>
@@ -403,19 +714,32 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
                               p32);
 }
 
+// The sliced form for direct and multi-destination write-backs up to their
+// size limits, the cooperative form otherwise.
+template <int DT, int NR, int WB>
+cudaError_t ll_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
+                        uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
+    if constexpr (WB != kPacketsOwn) {
+        const size_t bytes = count * Elem<DT>::kSize;
+        if (bytes <= (WB == kDirect ? kSliceDirectMaxBytes : kSliceMultiDestMaxBytes))
+            return slice_launch<DT, NR, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    }
+    return coop_dispatch<DT, NR, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+}
+
 template <int DT, int WB>
 cudaError_t coop_ranks(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
                        uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
     switch (nranks) {
-    case 1: return coop_dispatch<DT, 1, WB>(1, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    case 2: return coop_dispatch<DT, 2, WB>(2, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    case 4: return coop_dispatch<DT, 4, WB>(4, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    case 8: return coop_dispatch<DT, 8, WB>(8, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    case 16: return coop_dispatch<DT, 16, WB>(16, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    case 32: return coop_dispatch<DT, 32, WB>(32, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 1: return ll_dispatch<DT, 1, WB>(1, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 2: return ll_dispatch<DT, 2, WB>(2, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 4: return ll_dispatch<DT, 4, WB>(4, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 8: return ll_dispatch<DT, 8, WB>(8, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 16: return ll_dispatch<DT, 16, WB>(16, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+    case 32: return ll_dispatch<DT, 32, WB>(32, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
     default:
         if (nranks < 1 || nranks > SAR_MAX_RANKS) return cudaErrorInvalidValue;
-        return coop_dispatch<DT, 0, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
+        return ll_dispatch<DT, 0, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
     }
 }
 

@@ -252,7 +252,9 @@ slice_kernel(const RankPtrs p, int n_rt, size_t count, size_t nbytes, uint64_t m
                 st_slot4(row + slice_slot<SP>(4 * g), packet(x[u][0]), packet(x[u][1]));
                 st_slot4(row + slice_slot<SP>(4 * g + 2), packet(x[u][2]), packet(x[u][3]));
             } else {
-                for (int m = 0; m < 4 && 4 * g + m < np; ++m) st_slot(row + slice_slot<SP>(4 * g + m), packet(x[u][m]));
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (4 * g + m < np) st_slot(row + slice_slot<SP>(4 * g + m), packet(x[u][m]));
             }
         }
     }

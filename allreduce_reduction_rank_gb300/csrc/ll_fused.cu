@@ -1,6 +1,6 @@
 // ll_fused.cu -- sar_allreduce_ll_fused: the LL all-pair allreduce in one
-// cooperative launch, with the result written back directly from registers
-// (the kernel and its phases are described in ll_coop.cuh).
+// launch, with the result written back directly from registers (the kernels,
+// their phases and the choice between them are described in ll_coop.cuh).
 #include "ll_coop.cuh"
 
 namespace sar {

@@ -266,17 +266,20 @@ SAR_API sar_status sar_allreduce_ll_double(const void* const* in, void* const* o
                                            int32_t* d_status, sar_stream_t stream);
 
 /*
- * sar_allreduce_ll_fused -- the LL all-pair allreduce in one cooperative
- * launch: every block of simulated rank r packs its share of in[r] into
- * pkts[r] (the send), then polls its share of rank r's packet chunk in all N
- * packet buffers while other blocks are still packing, reduces in rank order
- * and writes to all N outputs (mscclpp commit history, the
- * allreduce_allpair_packet fix: send, reduce and write-back in the same
- * thread block).  Results equal sar_allreduce_ll's.
- *
- * The launch is cooperative (all blocks co-resident), so blocks may wait on
- * each other; a launch the device cannot make co-resident fails with
- * SAR_ERR_CUDA.
+ * sar_allreduce_ll_fused -- the LL all-pair allreduce in one launch (mscclpp
+ * commit history, the allreduce_allpair_packet fix: send, reduce and
+ * write-back in the same thread block).  Results equal sar_allreduce_ll's,
+ * and so does the packet image left in pkts.  Two forms:
+ *  - up to 256 KiB per rank (count * element size), block b plays every rank
+ *    for one slice of the packets: it packs the slice of every in[k] into
+ *    pkts[k], polls those packets (written by other warps of the block),
+ *    reduces in rank order and writes to all N outputs; no block waits for
+ *    another;
+ *  - above that, one cooperative launch: every block of simulated rank r
+ *    packs its share of in[r] into pkts[r], then polls its share of rank r's
+ *    packet chunk in all N packet buffers while other blocks are still
+ *    packing.  Blocks wait on each other, so all blocks must be co-resident;
+ *    a launch the device cannot make co-resident fails with SAR_ERR_CUDA.
  *
  * Epoch: with d_epoch == NULL the caller's `epoch` (non-zero, as in
  * sar_ll_pack).  Otherwise d_epoch is a caller-owned device epoch counter:
@@ -311,7 +314,7 @@ SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* ou
 
 /*
  * sar_allreduce_ll_writeback -- the LL all-pair allreduce with the write-back
- * as a second round of flagged packets, in one cooperative launch (mscclpp
+ * as a second round of flagged packets, in one launch (mscclpp
  * commit history: the allreduce_allpair_packet fix's send / reduce /
  * write-back, and the ReadPutPacket change that reads packet data once and
  * writes it to several destinations).
@@ -320,9 +323,12 @@ SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* ou
  * as packets (flag = epoch) into the result packet buffer `res` and then
  * polled again and unpacked into the outputs:
  *   multi_dest != 0 : each result packet is read once and written to all N
- *                     outputs (by the blocks of another rank than its reducer);
+ *                     outputs (by another warp of the block that reduced it
+ *                     up to 1 MiB per rank, in the sliced form of
+ *                     sar_allreduce_ll_fused; above, cooperatively, by the
+ *                     blocks of another rank than its reducer);
  *   multi_dest == 0 : every rank reads every result packet and writes its own
- *                     output (N reads per packet).
+ *                     output (N reads per packet; cooperative at every size).
  * Results equal sar_allreduce_ll's; after the call `res` holds the packets of
  * the reduced data, zero-padded like sar_ll_pack's.
  *

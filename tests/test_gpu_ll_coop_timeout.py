@@ -1,14 +1,18 @@
-"""The bounded polls of the cooperative LL kernels (sar_allreduce_ll_fused and
+"""The bounded polls of the one-launch LL kernels (sar_allreduce_ll_fused and
 sar_allreduce_ll_writeback in both fan-outs) running out.
 
-In one cooperative launch the packets a block polls are written by other
-blocks of the same launch, so with max_spins = 1 (one re-read) at 8 x 1 MiB
-the polls give up: the status word reads SAR_ERR_TIMEOUT, the launch ends,
-and the context stays usable.  The next call on the same buffers with the
-normal bound gives the oracle's outputs.  With the device epoch counter the
-counter still advances by one per launch, timed out or not, so the next
-launch gets a fresh epoch.  The failure is made by a short wait limit, the
-form of fault injection that leaves the GPU healthy."""
+In the cooperative form the packets a block polls are written by other
+blocks of the same launch, so with max_spins = 1 (one re-read) at 8 x 2 MiB
+(cooperative for every kind) the polls give up: the status word reads
+SAR_ERR_TIMEOUT, the launch ends, and the context stays usable.  The next
+call on the same buffers with the normal bound gives the oracle's outputs.
+With the device epoch counter the counter still advances by one per launch,
+timed out or not, so the next launch gets a fresh epoch.  The sliced form
+(direct write-back up to 256 KiB per rank, multi-destination up to 1 MiB)
+polls packets that warps of the same block have just written, so one
+re-read may or may not run out; its test checks what must hold either way.
+The failure is made by a short wait limit, the form of fault injection that
+leaves the GPU healthy."""
 import numpy as np
 import pytest
 import torch
@@ -38,12 +42,11 @@ def _call(sar, kind, gin, gout, pk, res, st, count, dt, max_spins, epoch=0, ctrl
                                        epoch_ctrl=ctrl, max_spins=max_spins, count=count, dtype=dt)
 
 
-@pytest.mark.parametrize("device_epoch", [False, True], ids=["host_epoch", "device_epoch"])
-@pytest.mark.parametrize("kind", KINDS)
-def test_coop_polls_run_out_and_the_next_call_is_exact(sar, kind, device_epoch):
-    wl = next(w for w in W.C5 if w.dtype == "fp32" and w.bytes_per_rank == 1 << 20)
-    n, count, dt = wl.nranks, wl.count, wl.dtype
-    ins = wl.inputs()
+def _short_bound_then_exact(sar, kind, device_epoch, bytes_per_rank, must_time_out):
+    n, dt = 8, "fp32"
+    count = bytes_per_rank // 4
+    rng = np.random.default_rng([bytes_per_rank, KINDS.index(kind), device_epoch])
+    ins = [(rng.random(count, dtype=np.float32) * 2 - 1).astype(np.float32) for _ in range(n)]
     want = oracle.allreduce(ins, dt)[0]
     gin = [Guarded.from_codes(c) for c in ins]
     gout = [Guarded(count * ESIZE[dt]) for _ in range(n)]
@@ -68,7 +71,8 @@ def test_coop_polls_run_out_and_the_next_call_is_exact(sar, kind, device_epoch):
         for g in pk:
             assert g.guards_intact()
         assert res.guards_intact()
-    assert timeouts > 0, "one re-read per poll never ran out at 8 x 1 MiB"
+    if must_time_out:
+        assert timeouts > 0, "one re-read per poll never ran out in the cooperative form"
     # the same context, the normal bound: exact again
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     for g in gout:
@@ -80,3 +84,15 @@ def test_coop_polls_run_out_and_the_next_call_is_exact(sar, kind, device_epoch):
         assert_same(g.codes(dt), want, dt)
     if device_epoch:
         assert sar.ll_device_epoch(ctrl) == launches
+
+
+@pytest.mark.parametrize("device_epoch", [False, True], ids=["host_epoch", "device_epoch"])
+@pytest.mark.parametrize("kind", KINDS)
+def test_coop_polls_run_out_and_the_next_call_is_exact(sar, kind, device_epoch):
+    _short_bound_then_exact(sar, kind, device_epoch, 2 << 20, must_time_out=True)
+
+
+@pytest.mark.parametrize("device_epoch", [False, True], ids=["host_epoch", "device_epoch"])
+@pytest.mark.parametrize("kind", ["fused", "writeback_multi_dest"])
+def test_sliced_polls_with_one_reread_and_the_next_call_is_exact(sar, kind, device_epoch):
+    _short_bound_then_exact(sar, kind, device_epoch, 256 << 10, must_time_out=False)

@@ -1,7 +1,9 @@
 """GPU parity of sar_allreduce_ll_fused (send, poll, reduce and write-back in
-one cooperative launch, so polls race against packing blocks) against the
-CPU oracle, through the C ABI; and the device-resident epoch counter that
-advances on every launch, including CUDA-graph replays."""
+one launch: sliced up to 256 KiB per rank, where each block polls packets
+its other warps have just written, cooperative above, where polls race
+against packing blocks) against the CPU oracle, through the C ABI; and the
+device-resident epoch counter that advances on every launch, including
+CUDA-graph replays."""
 import numpy as np
 import pytest
 import torch
@@ -173,3 +175,27 @@ def test_device_epoch_wraps_past_zero(sar, last, next_epoch):
     for g in gout:
         assert_same(g.codes(dt), want, dt)
     assert np.array_equal(pk[0].bytes(), oracle.ll_pack(ins, dt, next_epoch)[0])
+
+
+@pytest.mark.parametrize("n,dt,count", [(8, "fp32", 65536), (8, "fp32", 65537), (2, "bf16", 131072),
+                                        (2, "bf16", 131073), (32, "e4m3fn", 262144), (32, "e4m3fn", 262145)])
+def test_fused_on_both_sides_of_the_sliced_limit(sar, n, dt, count):
+    """256 KiB per rank runs sliced, one element more runs cooperatively:
+    both exact, and both leave the oracle's packet image."""
+    rng = np.random.default_rng([n, count, 5])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin = [Guarded.from_codes(c) for c in ins]
+    gout = [Guarded(count * ESIZE[dt], 0, fill=0x5A) for _ in range(n)]
+    pk = _packets(sar, n, count, dt)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sar.sar_allreduce_ll_fused([g.ptr for g in gin], [g.ptr for g in gout], [g.ptr for g in pk], st, epoch=3,
+                               count=count, dtype=dt)
+    assert sar.sar_read_device_status(st) == sar.SAR_OK
+    for g in gout:
+        assert_same(g.codes(dt), want, dt)
+        assert g.guards_intact()
+    want_pk = oracle.ll_pack(ins, dt, 3)
+    for r in range(n):
+        assert np.array_equal(pk[r].bytes(), want_pk[r])
+        assert pk[r].guards_intact()

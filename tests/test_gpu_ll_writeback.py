@@ -1,8 +1,10 @@
 """GPU parity of sar_allreduce_ll_writeback: the LL allreduce whose
-write-back is a second round of flagged packets (one cooperative launch),
-with each result packet either read once and written to every output
-(multi-destination) or read by every rank for its own output.  Outputs and
-the result-packet image are compared with the CPU oracle bit for bit."""
+write-back is a second round of flagged packets (one launch: sliced up to 1
+MiB per rank for the multi-destination fan-out, cooperative above and for
+the per-output fan-out), with each result packet either read once and
+written to every output (multi-destination) or read by every rank for its
+own output.  Outputs and the result-packet image are compared with the CPU
+oracle bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -142,3 +144,20 @@ def test_thousand_writeback_calls(sar, wl):
             for g in gout:
                 assert_same(g.codes(dt), want, dt, f"epoch {epoch}")
     assert sar.sar_read_device_status(st) == sar.SAR_OK
+
+
+@pytest.mark.parametrize("n,dt,count", [(8, "fp32", 262144), (8, "fp32", 262145), (2, "bf16", 524288),
+                                        (2, "bf16", 524289)])
+def test_multi_dest_on_both_sides_of_the_sliced_limit(sar, n, dt, count):
+    """1 MiB per rank runs sliced, one element more cooperatively: both give
+    the oracle's outputs and result-packet flags."""
+    rng = np.random.default_rng([n, count, 6])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout, pk, res = _run(sar, ins, dt, True, epoch=77)
+    for j, g in enumerate(gout):
+        assert_same(g.codes(dt), want, dt, f"out[{j}]")
+        assert g.guards_intact()
+    got_res = res.bytes().reshape(-1, 8)
+    assert np.all(got_res[:, 4:].copy().view(np.uint32).ravel() == 77)
+    assert res.guards_intact()
