@@ -105,11 +105,12 @@ typedef enum {
 } sar_status;
 
 /*
- * sar_allreduce -- the rsag allreduce.
+ * sar_allreduce -- the allreduce, by the rsag algorithm (fused or two-phase)
+ * or the LL all-pair algorithm.
  *
- * Defined by "Support 2 ranks in AllreduceRsAgZeroCopy - #948" ("why": the
- * ncclAllReduce that the rsag zero-copy algorithm serves; "what changed":
- * NPeers = NRanks - 1, peer loops unrolled at compile time).
+ * rsag is defined by "Support 2 ranks in AllreduceRsAgZeroCopy - #948"
+ * ("why": the ncclAllReduce that the rsag zero-copy algorithm serves; "what
+ * changed": NPeers = NRanks - 1, peer loops unrolled at compile time).
  *
  * For every element i and every rank j:
  *   out[j][i] = R( (((f32(in[0][i]) + f32(in[1][i])) + f32(in[2][i])) ... + f32(in[N-1][i])) )
