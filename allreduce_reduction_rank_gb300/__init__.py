@@ -236,7 +236,7 @@ def sar_allreduce_ll_double(ins, outs, pkts, epoch: int, status, max_spins: int 
 def sar_allreduce_ll_fused(ins, outs, pkts, status, epoch: int = 0, epoch_ctrl=None, max_spins: int = 1 << 20,
                            count=None, dtype=None, stream=None) -> None:
     """LL allreduce in one launch (sliced up to 256 KiB per rank, cooperative
-    above).  `epoch_ctrl`: optional device
+    above; see sar.h).  `epoch_ctrl`: optional device
     epoch counter (8 bytes, one uint64, zeroed once); when given, every launch
     takes the next epoch from it on the device (see ll_device_epoch)."""
     pin, n = _ptrs(ins)

@@ -354,22 +354,26 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
 //   C. kDirect: plain stores of the result to all N outputs; kPacketsAll: the
 //      result as flagged packets into `res`, then thread t polls the result
 //      packets another warp wrote and writes each, read once, to all N
-//      outputs.
+//      outputs; kPacketsOwn: the same result packets, then item (j, q) has
+//      output rank j read result group q (4 packets) and write output j, the
+//      items spread over the threads.
 // The packet and result-packet images are those of the cooperative form.
 // Measured against it (8 ranks fp32, CUDA graph, us per call, cooperative /
 // sliced): direct write-back 1 KiB 2.30 / 1.90, 64 KiB 2.89 / 2.18, 256 KiB
 // 3.72 / 3.04, 1 MiB 6.44 / 6.74; multi-destination packet write-back 1 KiB
 // 2.73 / 2.14, 256 KiB 4.56 / 3.48, 1 MiB 8.28 / 7.59, 4 MiB 26.6 / 44.2;
-// per-output packet write-back (result packets read once per output rank)
-// 1 KiB 2.72 / 2.91, 256 KiB 4.49 / 5.83, so that one stays cooperative.  4
-// packets per thread (16-byte stores, 128 registers) was slower at 1 MiB
+// per-output packet write-back (result packets read once per output rank,
+// the (rank, group) items spread over the threads) 1 KiB 2.87 / 2.59,
+// 16 KiB 3.24 / 2.84, 256 KiB 4.48 / 4.14, 1 MiB 8.16 / 8.90.  4 packets per
+// thread in the reduce (16-byte stores, 128 registers) was slower at 1 MiB
 // (7.38 us direct).
 // ---------------------------------------------------------------------------
 constexpr int kSliceThreads = 128;
 constexpr int kSlicePackets = 1;          // packets per thread and rank
-// Largest bytes per rank that run sliced.
+// Largest bytes per rank that run sliced (measured crossovers, 8 ranks fp32).
 constexpr size_t kSliceDirectMaxBytes = size_t(256) << 10;
 constexpr size_t kSliceMultiDestMaxBytes = size_t(1) << 20;
+constexpr size_t kSliceOwnMaxBytes = size_t(256) << 10;
 
 template <int N>
 __device__ __forceinline__ bool poll_slot(const uint64_t* src, int m_live, uint32_t epoch, uint64_t max_spins,
@@ -492,7 +496,6 @@ template <int DT, int NR, int WB, int PPT>
 __global__ void __launch_bounds__(kSliceThreads)
 slice_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t slices, uint32_t host_epoch,
              uint64_t* ctrl, uint64_t max_spins, int32_t* status, bool in16, bool out16, bool pk32) {
-    static_assert(WB == kDirect || WB == kPacketsAll, "the per-output write-back is cooperative only");
     constexpr int CT = kSliceThreads;
     constexpr int SP = PPT * CT;
     constexpr int G = SP / 4;
@@ -626,6 +629,30 @@ slice_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t slice
                                           r))
                     return;
             }
+        } else if constexpr (WB == kPacketsOwn) {
+            // Item (j, q): output rank j reads result group q (4 packets) of
+            // the slice and writes output j; the items are spread over the
+            // threads (rotated by a warp per output rank), the loads of up to
+            // 8 items issued before their polls.
+            const int ngr = (np + 3) / 4;
+            const int items = n * ngr;
+            for (int u0 = 0; u0 * CT < items; u0 += 8) {
+                uint64_t r[8][4];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int it = threadIdx.x + (u0 + u) * CT;
+                    const int j = it / ngr, q = (it + 32 * (j + 1)) % ngr;
+                    if (it < items) load_slot<4>(a.res, w0 + 4 * q, min(4, np - 4 * q), r[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int it = threadIdx.x + (u0 + u) * CT;
+                    const int j = it / ngr, q = (it + 32 * (j + 1)) % ngr;
+                    if (it < items && !finish_slot<DT, 4>(a, count, nbytes, w0 + 4 * q, min(4, np - 4 * q), j, j + 1,
+                                                          epoch, max_spins, status, out16, r[u]))
+                        return;
+                }
+            }
         }
     }
 }
@@ -719,11 +746,10 @@ cudaError_t coop_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t ep
 template <int DT, int NR, int WB>
 cudaError_t ll_dispatch(int nranks, const LLArgs& a, size_t count, uint32_t epoch, uint64_t* ctrl,
                         uint64_t max_spins, int32_t* status, bool in16, bool out16, cudaStream_t s) {
-    if constexpr (WB != kPacketsOwn) {
-        const size_t bytes = count * Elem<DT>::kSize;
-        if (bytes <= (WB == kDirect ? kSliceDirectMaxBytes : kSliceMultiDestMaxBytes))
-            return slice_launch<DT, NR, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
-    }
+    const size_t bytes = count * Elem<DT>::kSize;
+    const size_t limit = WB == kDirect ? kSliceDirectMaxBytes : (WB == kPacketsAll ? kSliceMultiDestMaxBytes : kSliceOwnMaxBytes);
+    if (bytes <= limit)
+        return slice_launch<DT, NR, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
     return coop_dispatch<DT, NR, WB>(nranks, a, count, epoch, ctrl, max_spins, status, in16, out16, s);
 }
 

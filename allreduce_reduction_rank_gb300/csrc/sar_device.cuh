@@ -316,13 +316,6 @@ template <> __device__ __forceinline__ void store_elem<SAR_FP8_E4M3B15>(void* ba
     static_cast<unsigned char*>(base)[i] = static_cast<unsigned char>(f32_to_e4m3b15(x));
 }
 
-// Widen element `e` of a 32-bit payload word (used by the LL tail).
-template <int DT> __device__ __forceinline__ float widen_one(uint32_t w, int e) {
-    float x[PerWord<DT>::kN];
-    widen_word<DT>(w, x);
-    return x[e];
-}
-
 // ---------------------------------------------------------------------------
 // Global-memory access with streaming cache hints.  Every byte of the rsag
 // inputs and outputs is touched exactly once, so nothing is kept in L1.

@@ -56,7 +56,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the rest of the 536.9 MB of outputs is still dirty in L2 when the launch
 # ends), valid while the kernel sources hash to `sources_sha`; otherwise
 # `traffic` is reported as null.
-TRAFFIC = {"sources_sha": "ac91b0bdef34e0e9", "bytes_per_launch": 1021750784}
+TRAFFIC = {"sources_sha": "365562bd70618ef1", "bytes_per_launch": 1022055424}
 KERNEL_SOURCES = ["allreduce_reduction_rank_gb300/csrc/rsag_kernels.cuh",
                   "allreduce_reduction_rank_gb300/csrc/rsag_fp16.cu",
                   "allreduce_reduction_rank_gb300/csrc/sar_device.cuh"]

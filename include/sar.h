@@ -329,7 +329,9 @@ SAR_API sar_status sar_allreduce_ll_fused(const void* const* in, void* const* ou
  *                     sar_allreduce_ll_fused; above, cooperatively, by the
  *                     blocks of another rank than its reducer);
  *   multi_dest == 0 : every rank reads every result packet and writes its own
- *                     output (N reads per packet; cooperative at every size).
+ *                     output (N reads per packet; sliced up to 256 KiB per
+ *                     rank, the (rank, packet group) reads spread over a
+ *                     block's threads; cooperative above).
  * Results equal sar_allreduce_ll's; after the call `res` holds the packets of
  * the reduced data, zero-padded like sar_ll_pack's.
  *

@@ -8,8 +8,8 @@ SAR_ERR_TIMEOUT, the launch ends, and the context stays usable.  The next
 call on the same buffers with the normal bound gives the oracle's outputs.
 With the device epoch counter the counter still advances by one per launch,
 timed out or not, so the next launch gets a fresh epoch.  The sliced form
-(direct write-back up to 256 KiB per rank, multi-destination up to 1 MiB)
-polls packets that warps of the same block have just written, so one
+(direct and per-output write-backs up to 256 KiB per rank, multi-destination
+up to 1 MiB) polls packets that warps of the same block have just written, so one
 re-read may or may not run out; its test checks what must hold either way.
 The failure is made by a short wait limit, the form of fault injection that
 leaves the GPU healthy."""
@@ -93,6 +93,6 @@ def test_coop_polls_run_out_and_the_next_call_is_exact(sar, kind, device_epoch):
 
 
 @pytest.mark.parametrize("device_epoch", [False, True], ids=["host_epoch", "device_epoch"])
-@pytest.mark.parametrize("kind", ["fused", "writeback_multi_dest"])
+@pytest.mark.parametrize("kind", KINDS)
 def test_sliced_polls_with_one_reread_and_the_next_call_is_exact(sar, kind, device_epoch):
     _short_bound_then_exact(sar, kind, device_epoch, 256 << 10, must_time_out=False)

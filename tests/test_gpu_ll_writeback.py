@@ -1,7 +1,7 @@
 """GPU parity of sar_allreduce_ll_writeback: the LL allreduce whose
 write-back is a second round of flagged packets (one launch: sliced up to 1
-MiB per rank for the multi-destination fan-out, cooperative above and for
-the per-output fan-out), with each result packet either read once and
+MiB per rank for the multi-destination fan-out and up to 256 KiB for the
+per-output one, cooperative above), with each result packet either read once and
 written to every output (multi-destination) or read by every rank for its
 own output.  Outputs and the result-packet image are compared with the CPU
 oracle bit for bit."""
@@ -160,4 +160,21 @@ def test_multi_dest_on_both_sides_of_the_sliced_limit(sar, n, dt, count):
         assert g.guards_intact()
     got_res = res.bytes().reshape(-1, 8)
     assert np.all(got_res[:, 4:].copy().view(np.uint32).ravel() == 77)
+    assert res.guards_intact()
+
+
+@pytest.mark.parametrize("n,dt,count", [(8, "fp32", 65536), (8, "fp32", 65537), (5, "bf16", 131072),
+                                        (5, "bf16", 131073)])
+def test_own_output_on_both_sides_of_the_sliced_limit(sar, n, dt, count):
+    """256 KiB per rank runs sliced, one element more cooperatively: both give
+    the oracle's outputs and result-packet flags."""
+    rng = np.random.default_rng([n, count, 7])
+    ins = [random_codes(rng, dt, count) for _ in range(n)]
+    want = oracle.allreduce(ins, dt)[0]
+    gin, gout, pk, res = _run(sar, ins, dt, False, epoch=78)
+    for j, g in enumerate(gout):
+        assert_same(g.codes(dt), want, dt, f"out[{j}]")
+        assert g.guards_intact()
+    got_res = res.bytes().reshape(-1, 8)
+    assert np.all(got_res[:, 4:].copy().view(np.uint32).ravel() == 78)
     assert res.guards_intact()
