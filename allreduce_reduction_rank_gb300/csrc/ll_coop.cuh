@@ -341,7 +341,7 @@ coop_kernel(const LLArgs a, int n_rt, size_t count, size_t nbytes, size_t chunk,
 }
 
 // ---------------------------------------------------------------------------
-// Sliced form (kDirect and kPacketsAll): block b plays every rank for packets
+// Sliced form: block b plays every rank for packets
 // [b*SP, (b+1)*SP) of the buffers (SP = PPT*kSliceThreads packets per rank),
 // so no block waits for another and the launch needs no co-residency.  In a
 // slice:
