@@ -236,7 +236,22 @@ def rsag_row(torch, sar, wl, dev, stream, l2_bytes, algo=0, calls=20, warm=5, gr
         want = rsag_result(torch, sar, din, wl, stream)
         row["outputs_ok"] = all(torch.equal(o.view(torch.uint8), want.view(torch.uint8)) for o in dout)
     del din, dout
+    if g is not None and algo == 0 and accum is None:
+        row["copy_graph_us"] = round(copy_floor_ms(torch, wl.nranks * wl.bytes_per_rank, dev, calls, stream) * 1e3, 3)
     return row
+
+
+def copy_floor_ms(torch, nbytes: int, dev, calls: int, stream) -> float:
+    """Context for a row: a device-to-device copy of the call's N*S bytes (N*S
+    read, N*S written, as the allreduce), timed the same way in a CUDA graph
+    (torch's same-type contiguous copy_, a cudaMemcpyAsync)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    with torch.cuda.stream(stream):
+        dst.copy_(src)
+    ms = time_graph(torch, lambda: dst.copy_(src), calls, stream)
+    del src, dst
+    return ms
 
 
 def rsag_result(torch, sar, din, wl, stream):
