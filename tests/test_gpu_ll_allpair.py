@@ -46,7 +46,7 @@ def _check(gin, gout, ins, want, dt, inplace=False):
 
 
 @pytest.mark.parametrize("count", [1, 3, 4097, 60001])
-@pytest.mark.parametrize("n", [2, 8, 32])
+@pytest.mark.parametrize("n", [1, 2, 8, 32])
 @pytest.mark.parametrize("dt", DTYPES)
 def test_ll_allpair_matches_oracle(sar, dt, n, count):
     rng = np.random.default_rng([DTYPES.index(dt), n, count, 77])
