@@ -1,6 +1,7 @@
 """The C ABI from a plain C program on the GPU: a C11 program that includes
 cuda_runtime.h and sar.h allocates 4 ranks of fp32 with the CUDA runtime, runs
-the fused rsag allreduce and the LL allreduce through libsar, and checks every
+the fused rsag allreduce, the LL allreduce with caller packet buffers and
+sar_allreduce with SAR_ALGO_LL_ALLPAIR through libsar, and checks every
 output element against the in-order binary32 sum it computes itself (exact:
 the inputs are multiples of 1/64 below 16 in magnitude)."""
 import os
@@ -88,6 +89,16 @@ int main(void) {
         return 5;
     }
     if (check(d_out, h, "ll")) return 6;
+
+    for (int r = 0; r < N; ++r)
+        if (cudaMemset(d_out[r], 0, COUNT * sizeof(float)) != cudaSuccess) return 2;
+    st = sar_allreduce(in, out, N, COUNT, SAR_FP32, SAR_ALGO_LL_ALLPAIR, NULL);
+    if (st != SAR_OK) {
+        printf("sar_allreduce (LL all-pair): %s\n", sar_status_string(st));
+        return 7;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return 7;
+    if (check(d_out, h, "ll_allpair")) return 8;
 
     for (int r = 0; r < N; ++r) {
         cudaFree(d_in[r]);
