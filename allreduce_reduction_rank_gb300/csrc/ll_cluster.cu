@@ -36,6 +36,8 @@
 // of the rank's packet range (chunk = packets per rank chunk, a multiple of
 // 4), cut at the end of the chunk and of the buffer.  Packet w holds bytes
 // 4w..4w+3 of a rank's input, zero past its end, as in sar_ll_pack.
+#include <atomic>
+
 #include "ll_packets.cuh"
 #include "sar_device.cuh"
 #include "sar_internal.h"
@@ -224,11 +226,20 @@ cudaError_t cluster_launch(int nranks, const RankPtrs& p, size_t count, size_t n
     const size_t teams = (chunk + CT - 1) / CT;
     if (teams * static_cast<size_t>(nranks) > 0x7FFFFFFFull) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(nranks) * CT * 8;
-    // Clusters above 8 CTAs are not portable: allowed explicitly.
+    // Clusters above 8 CTAs are not portable: allowed explicitly, once per
+    // device and kernel (only a successful call is remembered).
     if (nranks > 8) {
-        const cudaError_t e = cudaFuncSetAttribute(cluster_kernel<DT, NR, CT>,
-                                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        constexpr int kMaxDev = 64;
+        static std::atomic<bool> allowed[kMaxDev];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+        if (!allowed[dev].load(std::memory_order_acquire)) {
+            e = cudaFuncSetAttribute(cluster_kernel<DT, NR, CT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            allowed[dev].store(true, std::memory_order_release);
+        }
     }
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
