@@ -189,3 +189,14 @@ def test_golden_format_constants():
         codes = np.array([code], dtype=oracle.NP_STORAGE[oracle.DTYPES[fmt]])
         assert float(oracle.decode(codes, fmt)[0]) == value, (fmt, hex(code))
         assert int(oracle.round_f32(np.array([value], np.float32), fmt)[0]) == code, (fmt, value)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e4m3b15"])
+def test_fp8_nan_is_the_positive_all_ones_code(fmt):
+    """Reading of the pages' silence on NaN signs: narrowing any binary32 NaN
+    (either sign, any payload) to an fp8 format gives the one code S=0,
+    E=1111, M=111 (0x7F), which is NaN in both formats."""
+    nans = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFFFFFFFF], dtype=np.uint32).view(np.float32)
+    got = oracle.round_f32(nans, fmt)
+    assert np.all(got.astype(np.int64) == 0x7F), [hex(int(c)) for c in got]
+    assert np.isnan(oracle.decode(np.array([0x7F], dtype=np.uint8), fmt)[0])

@@ -65,6 +65,24 @@ MUTANTS = {
         ("if (flag != epoch) return ORC_NOT_ARRIVED;", "(void)flag;"),
     "unpack reads the payload from the flag half":
         ("rebuilt[r][at] = p[8 * (at / 4) + at % 4];", "rebuilt[r][at] = p[8 * (at / 4) + 4 + at % 4];"),
+    "e4m3fn subnormal scale":
+        ("    if (e == 0) mag = ldexpf((float)f, -9);", "    if (e == 0) mag = ldexpf((float)f, -8);"),
+    "packet count rounds down":
+        ("    return (bytes + 3) / 4;", "    return bytes / 4;"),
+    "e4m3b15 infinity decoded as NaN":
+        ("        if (f != 0) return bits_f32(0x7FC00000u);\n        mag = INFINITY;\n    } else if (e == 0) {\n"
+         "        mag = ldexpf((float)f, -17);",
+         "        return bits_f32(0x7FC00000u);\n    } else if (e == 0) {\n        mag = ldexpf((float)f, -17);"),
+    "reduce-scatter seeded with +0":
+        ("            float acc = orc_load(dt, in[0], i);\n            for (int k = 1; k < nranks; ++k) acc = acc + "
+         "orc_load(dt, in[k], i);\n            orc_store(dt, out[r], i, acc);",
+         "            float acc = 0.0f;\n            for (int k = 0; k < nranks; ++k) acc = acc + "
+         "orc_load(dt, in[k], i);\n            orc_store(dt, out[r], i, acc);"),
+    "e4m3fn NaN keeps its sign":
+        ("    if (isnan(x)) return 0x7F;\n    if (isinf(x)) return s | 0x7E;",
+         "    if (isnan(x)) return s | 0x7F;\n    if (isinf(x)) return s | 0x7E;"),
+    "fp16 overflow saturates instead of going to infinity":
+        ("    if (c < 0) return s | 0x7C00;", "    if (c < 0) return s | 0x7BFF;"),
 }
 
 
@@ -82,6 +100,8 @@ def _battery(points):
         lambda: ts.test_rank_order_is_0_to_n_minus_1(),
         lambda: [ts.test_rsag_chunks_partition_the_range(d) for d in ts.DTYPES],
         lambda: [ts.test_reduce_scatter_then_all_gather_is_allreduce(d, 8, 4097) for d in ts.DTYPES],
+        lambda: [ts.test_reduce_scatter_of_negative_zeros_is_negative_zero(d) for d in ts.DTYPES + ["e4m3b15"]],
+        lambda: [tf.test_fp8_nan_is_the_positive_all_ones_code(f) for f in ("e4m3fn", "e4m3b15")],
         lambda: [ts.test_ll_pack_byte_image(d, 5) for d in ts.DTYPES],
         lambda: [ts.test_ll_unpack_reduce_gives_the_exact_sums(d, 8, 257) for d in ts.DTYPES],
         lambda: ts.test_ll_stale_flag_is_not_arrived(),

@@ -67,6 +67,22 @@ def test_one_rank_is_identity(dt):
 
 
 @pytest.mark.parametrize("dt", DTYPES + ["e4m3b15"])
+def test_reduce_scatter_of_negative_zeros_is_negative_zero(dt):
+    """The in-order binary32 sum of -0 values is -0 (round to nearest: -0 + -0
+    = -0), so every chunk the reduce-scatter writes holds -0 codes, as the
+    allreduce's do (the seed is the first rank's value, not +0)."""
+    n, count = 4, 37
+    neg0 = {"bf16": 0x8000, "fp16": 0x8000, "fp32": np.float32(-0.0), "e4m3fn": 0x80, "e4m3b15": 0x80}[dt]
+    ins = [np.full(count, neg0, dtype=STORE[dt]) for _ in range(n)]
+    outs = [np.zeros(count, dtype=STORE[dt]) for _ in range(n)]
+    oracle.reduce_scatter(ins, outs, dt)
+    for r in range(n):
+        b, e = oracle.rsag_chunk(count, n, dt, r)
+        assert _same_bits(outs[r][b:e], ins[0][b:e]), r
+    assert _same_bits(oracle.allreduce(ins, dt)[0], ins[0])
+
+
+@pytest.mark.parametrize("dt", DTYPES + ["e4m3b15"])
 @pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 32])
 def test_all_equal_inputs_give_n_times_x(dt, n):
     rng = np.random.default_rng(n)
