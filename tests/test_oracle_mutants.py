@@ -83,6 +83,11 @@ MUTANTS = {
          "    if (isnan(x)) return s | 0x7F;\n    if (isinf(x)) return s | 0x7E;"),
     "fp16 overflow saturates instead of going to infinity":
         ("    if (c < 0) return s | 0x7C00;", "    if (c < 0) return s | 0x7BFF;"),
+    "conversion rounds twice, through bf16":
+        ("orc_store(dst_dt, dst, i, orc_load(src_dt, src, i));",
+         "orc_store(dst_dt, dst, i, orc_bf16_to_f32(orc_f32_to_bf16(orc_load(src_dt, src, i))));"),
+    "conversion decodes with the destination type":
+        ("orc_store(dst_dt, dst, i, orc_load(src_dt, src, i));", "orc_store(dst_dt, dst, i, orc_load(dst_dt, src, i));"),
 }
 
 
@@ -107,6 +112,9 @@ def _battery(points):
         lambda: ts.test_ll_stale_flag_is_not_arrived(),
         lambda: [ta.test_stepwise_reference(d, a, 8) for d, a in ta.CASES],
         lambda: ta.test_native_e4m3fn_rounds_every_partial_sum(),
+        lambda: ts.test_convert_e4m3fn_to_f32_every_code(),
+        lambda: [ts.test_convert_to_e4m3fn_rounds_once(d) for d in ("fp32", "bf16", "fp16")],
+        lambda: [ts.test_convert_from_e4m3fn_is_exact(d) for d in ("bf16", "fp16", "fp32")],
     ]
     failed = 0
     for c in checks:
