@@ -1,8 +1,11 @@
 """The oracle's pins have teeth: plausible mistakes planted in a copy of the
 oracle source (a wrong tie rule, a dropped rank, a reversed rank order, a
-lost sign, an off-by-one bias, a missing saturation, a wrong packet layout, an
-unrounded chunk size, a zero seed, an unpack that ignores the epoch or reads
-the wrong half of a packet) must each fail at least one pin.
+lost sign, an off-by-one bias or scale, a missing saturation, a wrong packet
+layout or count, an unrounded chunk size, a zero seed in the allreduce or the
+reduce-scatter, infinity decoded as NaN, a NaN code that keeps its sign, a
+conversion that rounds twice or decodes with the wrong type, an unpack that
+ignores the epoch or reads the wrong half of a packet) must each fail at
+least one pin.
 
 Mistakes are planted only in a temporary copy of the C oracle, on the CPU.
 """
