@@ -333,6 +333,7 @@ def test_graph_capture_and_replay(sar):
     gin = [Guarded.from_codes(c) for c in ins]
     gout = [Guarded(count * 2) for _ in range(n)]
     gout2 = [Guarded(count * 2) for _ in range(n)]
+    gout3 = [Guarded(count * 2) for _ in range(n)]
     s = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
@@ -341,10 +342,14 @@ def test_graph_capture_and_replay(sar):
         sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout2], count=count, dtype=dt, algo=1)
         with pytest.raises(sar.SarError):       # bad dtype: rejected before launch, capture unaffected
             sar.sar_allreduce([g.ptr for g in gin[:3]], [g.ptr for g in gout[:3]], count=count, dtype=9)
+        with pytest.raises(sar.SarError) as err:    # an unsupported rank count, the #948 failure mode
+            sar.sar_allreduce([gin[0].ptr] * 33, [gout[0].ptr] * 33, count=count, dtype=dt, algo=0)
+        assert err.value.status == sar.SAR_ERR_UNSUPPORTED_NRANKS
+        sar.sar_allreduce([g.ptr for g in gin], [g.ptr for g in gout3], count=count, dtype=dt, algo=2)
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
-    for g in gout + gout2:
+    for g in gout + gout2 + gout3:
         assert_same(g.codes(dt), want, dt)
         assert g.guards_intact()
 
